@@ -1,0 +1,495 @@
+"""Pins of the CPU oracle to things other than itself.
+
+Each test ties one oracle function to a format definition, a closed form,
+brute force on tiny inputs, exact rational arithmetic, a library routine or a
+layer invariant, so that a plausible mistake (a dropped term, a wrong sign or
+index, a transposed operand, a wrong rounding) fails at least one of them.
+"""
+
+import math
+from fractions import Fraction
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from oracle import formats as fm
+import synth
+
+F32 = np.float32
+
+
+# ------------------------------------------------------------------ helpers
+def exact_round_f32(q: Fraction) -> float:
+    """Round a rational to the nearest fp32 (ties to even), by integer search.
+
+    Written from the definition: find the binade, scale to a 24-bit integer
+    significand, round the remainder half to even.  Normal range only.
+    """
+    if q == 0:
+        return 0.0
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = a.numerator.bit_length() - a.denominator.bit_length()
+    # adjust so that 2^e <= a < 2^(e+1)
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    scaled = a / Fraction(2) ** (e - 23)          # in [2^23, 2^24)
+    m = scaled.numerator // scaled.denominator
+    rem = scaled - m
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and m % 2 == 1):
+        m += 1
+    return sign * float(m) * 2.0 ** (e - 23)
+
+
+def brute_nearest_e4m3(v: float) -> int:
+    """Nearest E4M3 code by exhaustive search over the finite codes; ties to even code;
+    saturating at 448; sign of zero kept."""
+    best = None
+    for code in range(256):
+        val = fm.E4M3_VALUES[code]
+        if np.isnan(val):
+            continue
+        if (code & 0x80) != (0x80 if math.copysign(1.0, v) < 0 else 0):
+            continue      # only codes of the same sign (so -0 is kept)
+        d = abs(val - v)
+        key = (d, code & 1)
+        if best is None or key < best[0]:
+            best = (key, code)
+    return best[1]
+
+
+# ----------------------------------------------------------- E4M3 format
+def test_e4m3_table_definition_points():
+    t = fm.E4M3_VALUES
+    assert t[0x7E] == 448.0 and t[0xFE] == -448.0
+    assert np.isnan(t[0x7F]) and np.isnan(t[0xFF])
+    assert t[0x08] == 2.0 ** -6            # smallest normal
+    assert t[0x01] == 2.0 ** -9            # smallest subnormal
+    assert t[0x07] == 7 / 8 * 2.0 ** -6    # largest subnormal
+    assert t[0x38] == 1.0                  # exponent field 7 = bias
+    assert t[0x00] == 0.0 and t[0x80] == 0.0 and math.copysign(1, t[0x80]) < 0
+    assert np.isfinite(t).sum() == 254
+    assert np.all(np.diff(t[:0x7F]) > 0)
+
+
+def test_e4m3_table_matches_torch():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    ref = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = fm.E4M3_VALUES
+    assert np.array_equal(np.isnan(ref), np.isnan(ours))
+    fin = ~np.isnan(ref)
+    assert np.array_equal(ref[fin], ours[fin])
+
+
+def test_e4m3_encode_roundtrip_all_codes():
+    codes = np.array([c for c in range(256) if c not in (0x7F, 0xFF)], np.uint8)
+    vals = fm.E4M3_VALUES[codes].astype(F32)
+    assert np.array_equal(fm.e4m3_encode(vals), codes)
+
+
+def _midpoint_probes():
+    pos = fm.E4M3_VALUES[:0x7F]
+    mids = ((pos[:-1] + pos[1:]) / 2).astype(F32)
+    probes = [mids, np.nextafter(mids, F32(np.inf)), np.nextafter(mids, F32(0))]
+    probes.append(pos.astype(F32))
+    v = np.concatenate(probes)
+    return np.concatenate([v, -v]).astype(F32)
+
+
+def test_e4m3_encode_brute_force():
+    rng = np.random.default_rng(1)
+    rand = np.concatenate([
+        rng.uniform(-464, 464, 3000),
+        rng.standard_normal(2000) * 2.0 ** rng.integers(-12, 9, 2000),
+        [449.0, 463.9, 464.0, 465.0, 1e6, -1e-12, 1e-12, 0.0, -0.0],
+    ]).astype(F32)
+    v = np.concatenate([_midpoint_probes(), rand])
+    ours = fm.e4m3_encode(v)
+    ref = np.array([brute_nearest_e4m3(float(x)) for x in v], np.uint8)
+    assert np.array_equal(ours, ref)
+
+
+def test_e4m3_encode_matches_torch_in_range():
+    rng = np.random.default_rng(2)
+    v = np.concatenate([_midpoint_probes(),
+                        rng.uniform(-448, 448, 200000).astype(F32),
+                        (rng.standard_normal(200000) * 0.01).astype(F32)])
+    v = v[np.abs(v) <= 448]
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert np.array_equal(fm.e4m3_encode(v), ref)
+
+
+def test_e4m3_saturation_and_nan():
+    v = np.array([448.5, 464.0, 480.0, 1e30, -500.0, np.inf, -np.inf, np.nan], F32)
+    assert list(fm.e4m3_encode(v)) == [0x7E, 0x7E, 0x7E, 0x7E, 0xFE, 0x7E, 0xFE, 0x7F]
+
+
+# ---------------------------------------------------------------- BF16
+def test_bf16_round_matches_torch():
+    rng = np.random.default_rng(3)
+    bits = rng.integers(0, 2 ** 32, 500000, dtype=np.uint64).astype(np.uint32)
+    v = bits.view(F32)
+    v = v[np.isfinite(v)]
+    ties = (((rng.integers(0, 2 ** 16, 1000).astype(np.uint32) << 16) | 0x8000)).view(F32)
+    v = np.concatenate([v, ties[np.isfinite(ties)], np.array([0.0, -0.0, 3.3895314e38], F32)])
+    ref = torch.from_numpy(v).to(torch.bfloat16).to(torch.float32).numpy()
+    ours = fm.bf16_round(v)
+    assert np.array_equal(ours.view(np.uint32), ref.view(np.uint32))
+
+
+# ------------------------------------------------------------ pow2 / UE8M0
+def test_pow2_ceil_against_frexp():
+    rng = np.random.default_rng(4)
+    s = (rng.uniform(0.5, 1.0, 20000) * 2.0 ** rng.integers(-30, 30, 20000)).astype(F32)
+    s = np.concatenate([s, (2.0 ** np.arange(-30, 30)).astype(F32)])
+    ours = fm.pow2_ceil(s)
+    for a, b in zip(s[::50].tolist() + s[-60:].tolist(), ours[::50].tolist() + ours[-60:].tolist()):
+        m, e = math.frexp(a)               # a = m * 2^e, m in [0.5, 1)
+        want = 2.0 ** (e - 1) if m == 0.5 else 2.0 ** e
+        assert b == want
+    assert np.all(ours >= s) and np.all(ours < 2 * s)
+    assert np.all((ours.view(np.uint32) & 0x7FFFFF) == 0)
+
+
+def test_ue8m0_bytes():
+    assert fm.ue8m0_to_f32(np.array([127, 128, 126, 110], np.uint8)).tolist() == [1.0, 2.0, 0.5, 2.0 ** -17]
+    assert fm.f32_exponent_field(np.array([1.0, 0.25, 2.0 ** -17], F32)).tolist() == [127, 125, 110]
+
+
+# --------------------------------------------------------------- fp32 FMA
+def test_fma_f32_exact_rational():
+    rng = np.random.default_rng(5)
+    a = (rng.standard_normal(3000) * 2.0 ** rng.integers(-20, 20, 3000)).astype(F32)
+    b = (rng.standard_normal(3000) * 2.0 ** rng.integers(-20, 20, 3000)).astype(F32)
+    c = (rng.standard_normal(3000) * 2.0 ** rng.integers(-20, 20, 3000)).astype(F32)
+    got = fm.fma_f32(a, b, c)
+    for x, y, z, g in zip(a.tolist(), b.tolist(), c.tolist(), got.tolist()):
+        want = exact_round_f32(Fraction(x) * Fraction(y) + Fraction(z))
+        assert g == want
+
+
+def test_fma_f32_double_rounding_case():
+    # exact value sits just below the tie between 1+2^-23 (odd) and 1+2^-22 (even);
+    # rounding through float64 first would land on the tie and pick the even side
+    a = F32(1 + 2.0 ** -23)
+    b = F32(2.0 ** -24 * (1 - 2.0 ** -23))
+    c = F32(1 + 2.0 ** -23)
+    want = exact_round_f32(Fraction(float(a)) * Fraction(float(b)) + Fraction(float(c)))
+    assert want == 1 + 2.0 ** -23
+    assert fm.fma_f32(a, b, c) == F32(want)
+    naive = F32(float(a) * float(b) + float(c))
+    assert naive != F32(want)          # the emulation matters here
+    # exact ties resolve to even
+    assert fm.fma_f32(F32(2.0 ** -12), F32(2.0 ** -12), F32(1.0)) == F32(1.0)
+
+
+# ------------------------------------------------------------------ scales
+def test_group_scale_closed_form():
+    amax = np.array([0.0, 448.0, 896.0, 1.0, 1e-9, 3.0], F32)
+    s = oracle.group_scale(amax, oracle.SCALE_FP32)
+    floor = F32(1.0) / F32(229376.0)
+    assert s[0] == floor and s[4] == floor
+    assert s[1] == 1.0 and s[2] == 2.0
+    assert s[3] == F32(1.0) / F32(448.0)
+    assert s[5] == F32(3.0) / F32(448.0)
+    p = oracle.group_scale(amax, oracle.SCALE_FP32_POW2)
+    assert p[1] == 1.0 and p[2] == 2.0
+    assert p[3] == 2.0 ** -8            # 1/448 = 2^-8.8 -> 2^-8
+    assert p[0] == 2.0 ** -17           # floor 2^-17.8 -> 2^-17
+    assert np.all(amax / p <= 448.0)
+
+
+def test_quant_1x128_properties():
+    rng = np.random.default_rng(6)
+    v = (rng.standard_normal((7, 512)) * 3).astype(F32)
+    v[2, 128:256] = 0.0
+    for fmt in (oracle.SCALE_FP32, oracle.SCALE_FP32_POW2, oracle.SCALE_UE8M0):
+        q, s = oracle.quant_1x128(v, fmt)
+        assert q.dtype == np.uint8 and s.shape == (7, 4)
+        assert np.all(q[2, 128:256] == 0) and s[2, 1] == oracle.group_scale(F32(0), fmt)
+        # each group: codes are the nearest E4M3 of v/s, the largest |code| <= 448
+        deq = oracle.e4m3_decode(q).reshape(7, 4, 128) * s[..., None]
+        g = v.reshape(7, 4, 128)
+        err = np.abs(deq - g)
+        assert np.all(err <= s[..., None] * np.maximum(np.abs(g / s[..., None]) * 2.0 ** -4, 2.0 ** -10) + 1e-30)
+        if fmt == oracle.SCALE_FP32:
+            # the group maximum maps to exactly 448 when the floor is not hit
+            top = np.abs(oracle.e4m3_decode(q)).reshape(7, 4, 128).max(-1)
+            assert np.all(top[s > oracle.SCALE_FLOOR] == 448.0)
+
+
+def test_quant_scaling_by_power_of_two():
+    rng = np.random.default_rng(7)
+    v = rng.standard_normal((3, 256)).astype(F32)
+    for fmt in (oracle.SCALE_FP32, oracle.SCALE_FP32_POW2):
+        q1, s1 = oracle.quant_1x128(v, fmt)
+        q2, s2 = oracle.quant_1x128(v * F32(8.0), fmt)
+        assert np.array_equal(q1, q2) and np.array_equal(s2, s1 * 8)
+
+
+# --------------------------------------------------------------- alignment
+def test_align_brute_force():
+    rng = np.random.default_rng(8)
+    for trial in range(60):
+        E = int(rng.integers(1, 12))
+        k = int(rng.integers(1, 5))
+        M = int(rng.integers(0, 40))
+        n = int(rng.integers(0, M + 1))
+        A = int(rng.choice([4, 8, 128]))
+        ids = rng.integers(-2, E + 2, (M, k)).astype(np.int32)
+        r = oracle.align(ids, n, E, A)
+        pairs = [(int(ids.reshape(-1)[p]), p) for p in range(n * k)
+                 if 0 <= ids.reshape(-1)[p] < E]
+        order = sorted(pairs)                         # by expert, then pair index
+        # rebuild expected layout by walking experts
+        seg, row = [], 0
+        exp_rows = {}
+        for e in range(E):
+            mine = [p for (ee, p) in order if ee == e]
+            seg.append(row)
+            for i, p in enumerate(mine):
+                exp_rows[p] = row + i
+            row += -(-len(mine) // A) * A
+        seg.append(row)
+        assert r["seg_start"].tolist() == seg
+        for p in range(n * k):
+            assert r["pair_row"][p] == exp_rows.get(p, -1)
+        for p, rr in exp_rows.items():
+            assert r["sorted_pair"][rr] == p
+        assert r["num_tiles"] == row // A
+        for i in range(r["num_tiles"]):
+            e = r["tile_expert"][i]
+            assert seg[e] <= i * A < seg[e + 1]
+        assert np.all(r["seg_start"] % A == 0)
+        assert (r["live_end"] - r["seg_start"][:-1]).sum() == len(pairs)
+
+
+def test_align_edge_cases():
+    ids = np.array([[-1, 5], [7, -3]], np.int32)
+    r = oracle.align(ids, 2, 4)
+    assert r["num_tiles"] == 0 and r["pair_row"].tolist() == [-1, -1, -1, -1]
+    r = oracle.align(np.zeros((0, 8), np.int32), 0, 72)
+    assert r["num_tiles"] == 0 and r["seg_start"].sum() == 0
+    # 128-pair threshold (16x8) and above (24x8), 72 experts (not a power of two)
+    rng = np.random.default_rng(9)
+    for M in (16, 24):
+        ids = np.stack([rng.permutation(72)[:8] for _ in range(M)]).astype(np.int32)
+        r = oracle.align(ids, M, 72)
+        assert (r["live_end"] - r["seg_start"][:-1]).sum() == M * 8
+        assert r["num_tiles"] == np.count_nonzero(np.bincount(ids.reshape(-1), minlength=72))
+
+
+# ------------------------------------------------------------- block GEMM
+def test_block_gemm_exact_integer_dot():
+    rng = np.random.default_rng(10)
+    aq = rng.integers(0, 256, (3, 128)).astype(np.uint8)
+    wq = rng.integers(0, 256, (128, 128)).astype(np.uint8)
+    aq[aq & 0x7F == 0x7F] = 0
+    wq[wq & 0x7F == 0x7F] = 0
+    acc = oracle.block_gemm(aq, np.ones((3, 1), F32), wq, np.ones((1, 1), F32))
+    # brute force: each E4M3 value times 2^9 is an integer
+    ia = np.rint(fm.E4M3_VALUES[aq] * 512).astype(object)
+    iw = np.rint(fm.E4M3_VALUES[wq] * 512).astype(object)
+    for r in range(3):
+        for c in range(0, 128, 7):
+            d = sum(int(x) * int(y) for x, y in zip(ia[r], iw[c]))
+            assert acc[r, c] == exact_round_f32(Fraction(d, 2 ** 18))
+
+
+def test_block_gemm_vs_dequantized_matmul():
+    rng = np.random.default_rng(11)
+    R, N, K = 5, 256, 512
+    aq = fm.e4m3_encode(rng.standard_normal((R, K)).astype(F32) * 100)
+    wq = fm.e4m3_encode(rng.standard_normal((N, K)).astype(F32) * 100)
+    a_s = rng.uniform(1e-3, 1e-2, (R, K // 128)).astype(F32)
+    w_s = rng.uniform(1e-3, 1e-2, (N // 128, K // 128)).astype(F32)
+    acc = oracle.block_gemm(aq, a_s, wq, w_s)
+    a_deq = fm.e4m3_decode(aq) * np.repeat(a_s.astype(np.float64), 128, axis=1)
+    w_deq = fm.e4m3_decode(wq) * np.repeat(np.repeat(w_s.astype(np.float64), 128, axis=0), 128, axis=1)
+    exact = a_deq @ w_deq.T
+    absterms = np.abs(fm.e4m3_decode(aq) * np.repeat(a_s.astype(np.float64), 128, 1)) @ \
+        np.abs(w_deq).T
+    bound = (K // 128 + 2) * 2.0 ** -23 * absterms
+    assert np.all(np.abs(acc - exact) <= bound)
+    # a transposed weight operand or a misplaced scale block breaks the match
+    w_s_t = np.ascontiguousarray(w_s[::-1])
+    bad = oracle.block_gemm(aq, a_s, wq, w_s_t)
+    assert np.any(np.abs(bad - exact) > bound)
+
+
+# ------------------------------------------------------------------ SwiGLU
+def test_swiglu_against_high_precision():
+    import mpmath
+    mpmath.mp.prec = 100
+    rng = np.random.default_rng(12)
+    g = fm.bf16_round((rng.standard_normal(400) * 4).astype(F32))
+    u = fm.bf16_round((rng.standard_normal(400) * 4).astype(F32))
+    h = oracle.swiglu(g, u)
+    for gi, ui, hi in zip(g.tolist(), u.tolist(), h.tolist()):
+        exact = mpmath.mpf(gi) / (1 + mpmath.exp(-mpmath.mpf(gi))) * ui
+        assert abs(hi - float(exact)) <= 4 * 2.0 ** -24 * abs(float(exact)) + 1e-45
+
+
+def test_swiglu_clamp_semantics():
+    g = np.array([10.0, -10.0, 3.0, 9.0], F32)
+    u = np.array([-9.0, 9.0, 2.0, 1.0], F32)
+    L = 7.0
+    sil = lambda z: z / (1 + math.exp(-z))
+    before = oracle.swiglu(g, u, oracle.CLAMP_BEFORE_SILU, L)
+    want_b = [sil(7.0) * -7.0, sil(-10.0) * 7.0, sil(3.0) * 2.0, sil(7.0) * 1.0]
+    after = oracle.swiglu(g, u, oracle.CLAMP_AFTER_SILU, L)
+    want_a = [min(sil(10.0), 7.0) * -7.0, sil(-10.0) * 7.0, sil(3.0) * 2.0, min(sil(9.0), 7.0) * 1.0]
+    none = oracle.swiglu(g, u, oracle.CLAMP_NONE, L)
+    want_n = [sil(10.0) * -9.0, sil(-10.0) * 9.0, sil(3.0) * 2.0, sil(9.0)]
+    np.testing.assert_allclose(before, want_b, rtol=1e-6)
+    np.testing.assert_allclose(after, want_a, rtol=1e-6)
+    np.testing.assert_allclose(none, want_n, rtol=1e-6)
+
+
+# ---------------------------------------------------------------- reduce
+def test_topk_reduce_hand_example():
+    y = np.array([[[1.0, 2.0], [4.0, -8.0], [100.0, 100.0]]], F32)
+    w = np.array([[0.5, 0.25, 0.125]], F32)
+    present = np.array([[True, True, False]])
+    out = oracle.topk_reduce(y, w, present)
+    assert out.tolist() == [[1.5, -1.0]]
+    # fp32 accumulation then one BF16 rounding: 1 + 2^-9 is not a BF16 value
+    y = np.array([[[1.0], [2.0 ** -9]]], F32)
+    out = oracle.topk_reduce(y, np.ones((1, 2), F32), np.ones((1, 2), bool))
+    assert out[0, 0] == 1.0
+
+
+# ----------------------------------------------------------- layer pins
+@pytest.fixture(scope="module")
+def small_case():
+    shape = synth.small_shape(E=6, H=256, I=256, topk=2)
+    return synth.make_case("small", 12, shape=shape)
+
+
+def _fwd(case, **kw):
+    w = case.weights
+    sh = case.shape
+    args = dict(act_fmt=sh.act_fmt, weight_fmt=sh.weight_fmt,
+                clamp_mode=sh.clamp_mode, limit=sh.limit)
+    args.update(kw)
+    return oracle.moe_forward(case.x, case.topk_ids, case.topk_weights,
+                              w.w13, w.s13, w.w2, w.s2, **args)
+
+
+def dense_reference(case, clamp_mode=0, limit=0.0):
+    """Unquantized-activation layer in float64 with the dequantized weights."""
+    w = case.weights
+    out = np.zeros(case.x.shape, np.float64)
+    I = w.w13.shape[1] // 2
+    for t in range(case.x.shape[0]):
+        for j in range(case.topk_ids.shape[1]):
+            e = case.topk_ids[t, j]
+            if not (0 <= e < w.w13.shape[0]):
+                continue
+            w13 = fm.e4m3_decode(w.w13[e]) * np.kron(oracle.weight_scales_f32(w.s13[e], case.shape.weight_fmt), np.ones((128, 128)))
+            w2 = fm.e4m3_decode(w.w2[e]) * np.kron(oracle.weight_scales_f32(w.s2[e], case.shape.weight_fmt), np.ones((128, 128)))
+            g1 = w13 @ case.x[t].astype(np.float64)
+            g, u = g1[:I], g1[I:]
+            if clamp_mode == 1:
+                g = np.minimum(g, limit); u = np.clip(u, -limit, limit)
+            h = g / (1 + np.exp(-g))
+            if clamp_mode == 2:
+                h = np.minimum(h, limit); u = np.clip(u, -limit, limit)
+            out[t] += case.topk_weights[t, j] * (w2 @ (h * u))
+    return out
+
+
+def test_layer_close_to_dense_reference(small_case):
+    out = _fwd(small_case)
+    ref = dense_reference(small_case)
+    rel = np.linalg.norm(out - ref) / np.linalg.norm(ref)
+    # FP8 activation rounding (3 mantissa bits) dominates: a few percent
+    assert 0.002 < rel < 0.1, rel
+
+
+def test_layer_invariants(small_case):
+    c = small_case
+    base = _fwd(c)
+    # doubling the routing weights doubles the output exactly
+    w2x = synth.LayerCase(c.shape, c.M_cap, c.n, c.x_bits, c.x, c.topk_ids,
+                          c.topk_weights * 2, c.weights)
+    assert np.array_equal(_fwd(w2x), base * 2)
+    # all ids dropped -> zero output
+    dropped = synth.LayerCase(c.shape, c.M_cap, c.n, c.x_bits, c.x,
+                              np.full_like(c.topk_ids, -1), c.topk_weights, c.weights)
+    assert np.all(_fwd(dropped) == 0)
+    # experts that no pair routes to contribute nothing: change their weights
+    used = set(c.topk_ids.reshape(-1).tolist())
+    unused = [e for e in range(c.shape.E) if e not in used]
+    if unused:
+        w = c.weights
+        w13 = w.w13.copy(); w13[unused] = 0x38
+        alt = synth.LayerCase(c.shape, c.M_cap, c.n, c.x_bits, c.x, c.topk_ids, c.topk_weights,
+                              synth.Weights(w13, w.s13, w.w2, w.s2))
+        assert np.array_equal(_fwd(alt), base)
+    # token order does not matter
+    perm = np.random.default_rng(0).permutation(c.M_cap)
+    pc = synth.LayerCase(c.shape, c.M_cap, c.n, c.x_bits[perm], c.x[perm], c.topk_ids[perm],
+                         c.topk_weights[perm], c.weights)
+    assert np.array_equal(_fwd(pc), base[perm])
+
+
+def test_one_live_row_single_expert(small_case):
+    """topk = 1 with weight 1: the output is the BF16 expert output itself,
+    and equals the dequantized-weight dense FFN to within FP8 activation error."""
+    c = small_case
+    ids = c.topk_ids[:1, :1].copy()
+    one = synth.LayerCase(c.shape, 1, 1, c.x_bits[:1], c.x[:1], ids,
+                          np.ones((1, 1), F32), c.weights)
+    out = _fwd(one)
+    ref = dense_reference(one)
+    assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 0.1
+    w = c.weights
+    e = ids[0, 0]
+    y = oracle.expert_rows(c.x[:1], w.w13[e], w.s13[e], w.w2[e], w.s2[e], 0, 0)
+    assert np.array_equal(out, y)
+
+
+def test_clamp_modes_against_dense(small_case):
+    c = small_case
+    for mode in (1, 2):
+        out = _fwd(c, clamp_mode=mode, limit=0.05)
+        ref = dense_reference(c, mode, 0.05)
+        assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 0.1
+    # a limit that clamps does change the result
+    assert not np.array_equal(_fwd(c, clamp_mode=1, limit=0.05), _fwd(c))
+
+
+def test_pow2_scales_no_better_than_fp32(small_case):
+    """Power-of-two activation scales add rounding error (vLLM per-layer scale
+    page, Claims): on average the layer error is not lower than with fp32 scales."""
+    c = small_case
+    ref = dense_reference(c)
+    e32 = np.linalg.norm(_fwd(c, act_fmt=0) - ref)
+    ep2 = np.linalg.norm(_fwd(c, act_fmt=1) - ref)
+    assert ep2 >= 0.9 * e32
+
+
+def test_planted_mistakes_are_caught(monkeypatch, small_case):
+    """A mistake planted in the oracle (on the CPU) must fail a pin."""
+    from oracle import moe_ref
+    c = small_case
+    ref = dense_reference(c)
+    good = np.linalg.norm(_fwd(c) - ref) / np.linalg.norm(ref)
+    # swapped gate/up halves
+    orig = moe_ref.swiglu
+    monkeypatch.setattr(moe_ref, "swiglu", lambda g, u, m=0, l=0.0: orig(u, g, m, l))
+    bad = np.linalg.norm(_fwd(c) - ref) / np.linalg.norm(ref)
+    monkeypatch.setattr(moe_ref, "swiglu", orig)
+    assert good < 0.1 <= bad          # the dense-reference pin's bound
+    # weight scale block indexed transposed
+    orig_ws = moe_ref.weight_scales_f32
+    monkeypatch.setattr(moe_ref, "weight_scales_f32",
+                        lambda s, f: np.ascontiguousarray(np.asarray(orig_ws(s, f))[::-1, ::-1]))
+    bad = np.linalg.norm(_fwd(c) - ref) / np.linalg.norm(ref)
+    monkeypatch.setattr(moe_ref, "weight_scales_f32", orig_ws)
+    assert good < 0.1 <= bad
