@@ -1,0 +1,390 @@
+// Host side of the C ABI: argument validation, the workspace plan, TMA tensor maps and the launch
+// sequence of one layer forward.  Nothing here allocates device memory or synchronizes the host
+// (except moe_last_device_status, which exists to read the device status word).
+#include <string.h>
+
+#include <algorithm>
+#include <mutex>
+
+#include "moe_internal.h"
+
+namespace moe {
+
+static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+// FC1 K-split for small batches: enough CTAs to stream the occupied experts' weights from HBM.
+// Upper bound of live tiles = min(E, P_cap); target about two CTAs per SM of a 152-SM part.
+static int choose_fc1_ksplit(int E, int H, int I, int P_cap) {
+  if (P_cap > 1024) return 1;
+  const long items = (long)std::min(E, P_cap) * (I / kGroup);
+  const int kb = H / kGroup;
+  int ks = 1;
+  while (ks < 8 && items * ks * 2 <= 304 && kb % (ks * 2) == 0) ks *= 2;
+  return ks;
+}
+
+static moe_status check_shape(int M_cap, int E, int H, int I, int topk, int act_fmt) {
+  if (M_cap < 0 || E <= 0 || H <= 0 || I <= 0 || topk <= 0) return MOE_ERR_INVALID_ARG;
+  if (act_fmt < MOE_SCALE_FP32 || act_fmt > MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+  if (H % kGroup || I % kGroup || H > 32768 || I > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if (topk > kMaxTopk || E > kMaxExperts) return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)M_cap * topk > kMaxPairs) return MOE_ERR_UNSUPPORTED_SHAPE;
+  return MOE_OK;
+}
+
+moe_status make_plan(int M_cap, int E, int H, int I, int topk, int act_fmt, Plan* plan) {
+  const moe_status st = check_shape(M_cap, E, H, I, topk, act_fmt);
+  if (st != MOE_OK) return st;
+  memset(plan, 0, sizeof(*plan));
+  moe_ws_plan& w = plan->ws;
+  const long long P_cap = (long long)M_cap * topk;
+  const long long pad_rows = P_cap + (long long)std::min<long long>(E, P_cap) * (kAlign - 1);
+  const long long R_cap = (pad_rows + kAlign - 1) / kAlign * kAlign;
+  w.P_cap = (int32_t)P_cap;
+  w.R_cap = (int32_t)R_cap;
+  w.T_cap = (int32_t)(R_cap / kAlign);
+  w.fc1_ksplit = choose_fc1_ksplit(E, H, I, (int)P_cap);
+  const size_t sc = act_fmt == MOE_SCALE_UE8M0 ? 1 : 4;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  w.status = take(4);
+  w.num_tiles = take(4);
+  w.seg_start = take((size_t)(E + 1) * 4);
+  w.live_end = take((size_t)E * 4);
+  w.sorted_pair = take((size_t)R_cap * 4);
+  w.pair_row = take((size_t)P_cap * 4);
+  w.tile_expert = take((size_t)w.T_cap * 4);
+  w.a1_q = take((size_t)R_cap * H);
+  w.a1_s = take((size_t)(H / kGroup) * R_cap * sc);
+  w.a2_q = take((size_t)R_cap * I);
+  w.a2_s = take((size_t)(I / kGroup) * R_cap * sc);
+  w.y = take((size_t)R_cap * H * 2);
+  w.splitk_partial = take(w.fc1_ksplit > 1 ? (size_t)w.fc1_ksplit * P_cap * 2 * I * 4 : 0);
+  w.splitk_count = take(w.fc1_ksplit > 1 ? (size_t)w.T_cap * (I / kGroup) * 4 : 0);
+  w.total_bytes = off;
+  plan->M_cap = M_cap;
+  plan->E = E;
+  plan->H = H;
+  plan->I = I;
+  plan->topk = topk;
+  plan->act_fmt = act_fmt;
+  return MOE_OK;
+}
+
+// ------------------------------------------------------------- tensor maps
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Byte matrix [outer][inner] (row stride = inner bytes), boxes of box_outer rows x 128 bytes with
+// the 128-byte swizzle the MMA descriptors expect.
+static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                        uint32_t box_outer) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, outer};
+  const cuuint64_t strides[1] = {inner};
+  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    return 148;
+  return n;
+}
+
+// ------------------------------------------------------------ validation
+static bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+static moe_status check_ws(const Plan& pl, const void* ws, size_t ws_bytes) {
+  if (ws == nullptr || !aligned(ws, 256)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < pl.ws.total_bytes) return MOE_ERR_WORKSPACE_TOO_SMALL;
+  return MOE_OK;
+}
+
+static moe_status check_args(const moe_fwd_args* a, const void* ws, size_t ws_bytes, Plan* pl,
+                             bool need_x, bool need_w13, bool need_w2, bool need_reduce) {
+  if (a == nullptr) return MOE_ERR_INVALID_ARG;
+  if (a->weight_scale_fmt < MOE_SCALE_FP32 || a->weight_scale_fmt > MOE_SCALE_UE8M0)
+    return MOE_ERR_INVALID_ARG;
+  if (a->clamp_mode < MOE_CLAMP_NONE || a->clamp_mode > MOE_CLAMP_AFTER_SILU)
+    return MOE_ERR_INVALID_ARG;
+  if (a->clamp_mode != MOE_CLAMP_NONE && !(a->clamp_limit >= 0.0f && a->clamp_limit < 3.4e38f))
+    return MOE_ERR_INVALID_ARG;
+  moe_status st = make_plan(a->M_cap, a->E, a->H, a->I, a->topk, a->act_scale_fmt, pl);
+  if (st != MOE_OK) return st;
+  st = check_ws(*pl, ws, ws_bytes);
+  if (st != MOE_OK) return st;
+  const size_t wsc = a->weight_scale_fmt == MOE_SCALE_UE8M0 ? 1 : 4;
+  if (a->d_num_tokens != nullptr && !aligned(a->d_num_tokens, 4)) return MOE_ERR_INVALID_ARG;
+  if (need_x) {
+    if (a->x == nullptr || !aligned(a->x, 16)) return MOE_ERR_INVALID_ARG;
+    if (a->topk_ids == nullptr || !aligned(a->topk_ids, 4)) return MOE_ERR_INVALID_ARG;
+  }
+  if (need_w13) {
+    if (a->w13 == nullptr || !aligned(a->w13, 16)) return MOE_ERR_INVALID_ARG;
+    if (a->s13 == nullptr || !aligned(a->s13, wsc)) return MOE_ERR_INVALID_ARG;
+  }
+  if (need_w2) {
+    if (a->w2 == nullptr || !aligned(a->w2, 16)) return MOE_ERR_INVALID_ARG;
+    if (a->s2 == nullptr || !aligned(a->s2, wsc)) return MOE_ERR_INVALID_ARG;
+  }
+  if (need_reduce) {
+    if (a->topk_weights == nullptr || !aligned(a->topk_weights, 4)) return MOE_ERR_INVALID_ARG;
+    if (a->out == nullptr || !aligned(a->out, 16)) return MOE_ERR_INVALID_ARG;
+  }
+  return MOE_OK;
+}
+
+template <typename T>
+static T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+// ------------------------------------------------------------- steps
+static moe_status run_align(const int32_t* ids, const int32_t* d_n, const Plan& pl, void* ws,
+                            cudaStream_t s) {
+  AlignParams p;
+  p.topk_ids = ids;
+  p.d_num_tokens = d_n;
+  p.M_cap = pl.M_cap;
+  p.topk = pl.topk;
+  p.E = pl.E;
+  p.seg_start = at<int32_t>(ws, pl.ws.seg_start);
+  p.live_end = at<int32_t>(ws, pl.ws.live_end);
+  p.sorted_pair = at<int32_t>(ws, pl.ws.sorted_pair);
+  p.pair_row = at<int32_t>(ws, pl.ws.pair_row);
+  p.tile_expert = at<int32_t>(ws, pl.ws.tile_expert);
+  p.num_tiles = at<int32_t>(ws, pl.ws.num_tiles);
+  p.status = at<int32_t>(ws, pl.ws.status);
+  p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
+  p.splitk_count_len = pl.ws.fc1_ksplit > 1 ? pl.ws.T_cap * (pl.I / kGroup) : 0;
+  return launch_align(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static moe_status run_quant(const void* x, const int32_t* d_n, const Plan& pl, void* ws,
+                            cudaStream_t s) {
+  if (pl.M_cap == 0) return MOE_OK;
+  QuantParams p;
+  p.x = static_cast<const uint16_t*>(x);
+  p.d_num_tokens = d_n;
+  p.pair_row = at<int32_t>(ws, pl.ws.pair_row);
+  p.M_cap = pl.M_cap;
+  p.H = pl.H;
+  p.topk = pl.topk;
+  p.R_cap = pl.ws.R_cap;
+  p.fmt = pl.act_fmt;
+  p.a_q = at<uint8_t>(ws, pl.ws.a1_q);
+  p.a_s = at<void>(ws, pl.ws.a1_s);
+  return launch_quant(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static void fill_gemm_common(GemmParams& p, const Plan& pl, void* ws) {
+  memset(&p, 0, sizeof(p));
+  p.tile_expert = at<int32_t>(ws, pl.ws.tile_expert);
+  p.num_tiles = at<int32_t>(ws, pl.ws.num_tiles);
+  p.live_end = at<int32_t>(ws, pl.ws.live_end);
+  p.R_cap = pl.ws.R_cap;
+  p.status = at<int32_t>(ws, pl.ws.status);
+  p.act_fmt = pl.act_fmt;
+  p.a_scale_ue8m0 = pl.act_fmt == MOE_SCALE_UE8M0;
+  p.P_cap = pl.ws.P_cap;
+  p.sorted_pair = at<int32_t>(ws, pl.ws.sorted_pair);
+}
+
+static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {
+  if (pl.ws.R_cap == 0) return MOE_OK;
+  CUtensorMap tmA, tmB;
+  if (!make_map_u8(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kABoxRows) ||
+      !make_map_u8(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup))
+    return MOE_ERR_CUDA;
+  GemmParams p;
+  fill_gemm_common(p, pl, ws);
+  p.a_scale = at<void>(ws, pl.ws.a1_s);
+  p.b_scale = a->s13;
+  p.b_scale_ue8m0 = a->weight_scale_fmt == MOE_SCALE_UE8M0;
+  p.K = pl.H;
+  p.n_blocks = pl.I / kGroup;
+  p.b_rows_per_expert = 2 * pl.I;
+  p.out_cols = pl.I;
+  p.ksplit = pl.ws.fc1_ksplit;
+  p.a2_q = at<uint8_t>(ws, pl.ws.a2_q);
+  p.a2_s = at<void>(ws, pl.ws.a2_s);
+  p.clamp_mode = a->clamp_mode;
+  p.clamp_limit = a->clamp_limit;
+  p.splitk_partial = at<float>(ws, pl.ws.splitk_partial);
+  p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
+  const long items = (long)pl.ws.T_cap * p.n_blocks * p.ksplit;
+  const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
+  return launch_fc1(tmA, tmB, p, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {
+  if (pl.ws.R_cap == 0) return MOE_OK;
+  CUtensorMap tmA, tmB;
+  if (!make_map_u8(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kABoxRows) ||
+      !make_map_u8(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup))
+    return MOE_ERR_CUDA;
+  GemmParams p;
+  fill_gemm_common(p, pl, ws);
+  p.a_scale = at<void>(ws, pl.ws.a2_s);
+  p.b_scale = a->s2;
+  p.b_scale_ue8m0 = a->weight_scale_fmt == MOE_SCALE_UE8M0;
+  p.K = pl.I;
+  p.n_blocks = (pl.H + kBN - 1) / kBN;
+  p.b_rows_per_expert = pl.H;
+  p.out_cols = pl.H;
+  p.ksplit = 1;
+  p.y = at<uint16_t>(ws, pl.ws.y);
+  const long items = (long)pl.ws.T_cap * p.n_blocks;
+  const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
+  return launch_fc2(tmA, tmB, p, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+static moe_status run_reduce(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {
+  if (pl.M_cap == 0) return MOE_OK;
+  ReduceParams p;
+  p.y = at<uint16_t>(ws, pl.ws.y);
+  p.pair_row = at<int32_t>(ws, pl.ws.pair_row);
+  p.topk_weights = a->topk_weights;
+  p.d_num_tokens = a->d_num_tokens;
+  p.M_cap = pl.M_cap;
+  p.H = pl.H;
+  p.topk = pl.topk;
+  p.out = static_cast<uint16_t*>(a->out);
+  return launch_reduce(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+moe_status moe_workspace_plan(int M_cap, int E, int H, int I, int topk, moe_scale_fmt act_fmt,
+                              moe_ws_plan* plan) {
+  if (plan == nullptr) return MOE_ERR_INVALID_ARG;
+  Plan pl;
+  const moe_status st = make_plan(M_cap, E, H, I, topk, act_fmt, &pl);
+  if (st == MOE_OK) *plan = pl.ws;
+  return st;
+}
+
+size_t moe_workspace_bytes(int M_cap, int E, int H, int I, int topk, moe_scale_fmt act_fmt) {
+  Plan pl;
+  return make_plan(M_cap, E, H, I, topk, act_fmt, &pl) == MOE_OK ? pl.ws.total_bytes : 0;
+}
+
+moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M_cap, int topk, int E,
+                     int H, int I, moe_scale_fmt act_fmt, void* workspace, size_t workspace_bytes,
+                     moe_stream_t stream) {
+  Plan pl;
+  moe_status st = make_plan(M_cap, E, H, I, topk, act_fmt, &pl);
+  if (st != MOE_OK) return st;
+  st = check_ws(pl, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (M_cap > 0 && (topk_ids == nullptr || !aligned(topk_ids, 4))) return MOE_ERR_INVALID_ARG;
+  if (d_num_tokens != nullptr && !aligned(d_num_tokens, 4)) return MOE_ERR_INVALID_ARG;
+  return run_align(topk_ids, d_num_tokens, pl, workspace, (cudaStream_t)stream);
+}
+
+moe_status moe_quant_act(const void* x_bf16, const int32_t* d_num_tokens, int M_cap, int E, int H,
+                         int I, int topk, moe_scale_fmt act_fmt, void* workspace,
+                         size_t workspace_bytes, moe_stream_t stream) {
+  Plan pl;
+  moe_status st = make_plan(M_cap, E, H, I, topk, act_fmt, &pl);
+  if (st != MOE_OK) return st;
+  st = check_ws(pl, workspace, workspace_bytes);
+  if (st != MOE_OK) return st;
+  if (M_cap > 0 && (x_bf16 == nullptr || !aligned(x_bf16, 16))) return MOE_ERR_INVALID_ARG;
+  if (d_num_tokens != nullptr && !aligned(d_num_tokens, 4)) return MOE_ERR_INVALID_ARG;
+  return run_quant(x_bf16, d_num_tokens, pl, workspace, (cudaStream_t)stream);
+}
+
+moe_status moe_fc1_swiglu_quant(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream) {
+  Plan pl;
+  const moe_status st = check_args(args, workspace, workspace_bytes, &pl, false, true, false, false);
+  if (st != MOE_OK) return st;
+  return run_fc1(args, pl, workspace, (cudaStream_t)stream);
+}
+
+moe_status moe_fc2(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                   moe_stream_t stream) {
+  Plan pl;
+  const moe_status st = check_args(args, workspace, workspace_bytes, &pl, false, false, true, false);
+  if (st != MOE_OK) return st;
+  return run_fc2(args, pl, workspace, (cudaStream_t)stream);
+}
+
+moe_status moe_topk_reduce(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream) {
+  Plan pl;
+  const moe_status st = check_args(args, workspace, workspace_bytes, &pl, false, false, false, true);
+  if (st != MOE_OK) return st;
+  return run_reduce(args, pl, workspace, (cudaStream_t)stream);
+}
+
+moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream) {
+  Plan pl;
+  moe_status st = check_args(args, workspace, workspace_bytes, &pl, true, true, true, true);
+  if (st != MOE_OK) return st;
+  if (pl.M_cap == 0) return MOE_OK;
+  const cudaStream_t s = (cudaStream_t)stream;
+  if ((st = run_align(args->topk_ids, args->d_num_tokens, pl, workspace, s)) != MOE_OK) return st;
+  if ((st = run_quant(args->x, args->d_num_tokens, pl, workspace, s)) != MOE_OK) return st;
+  if ((st = run_fc1(args, pl, workspace, s)) != MOE_OK) return st;
+  if ((st = run_fc2(args, pl, workspace, s)) != MOE_OK) return st;
+  return run_reduce(args, pl, workspace, s);
+}
+
+moe_status moe_last_device_status(const void* workspace, moe_stream_t stream) {
+  if (workspace == nullptr || !aligned(workspace, 256)) return MOE_ERR_INVALID_ARG;
+  int32_t v = 0;
+  if (cudaStreamSynchronize((cudaStream_t)stream) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemcpy(&v, workspace, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return (v == 0) ? MOE_OK : (moe_status)v;
+}
+
+const char* moe_status_str(moe_status status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+    case MOE_ERR_WORKSPACE_TOO_SMALL: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device-side wait timed out";
+  }
+  return "unknown status";
+}
+
+const char* moe_version(void) { return "block_fp8_mixture_gb300 0.1 (sm_103a)"; }
+
+}  // extern "C"

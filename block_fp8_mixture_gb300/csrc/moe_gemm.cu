@@ -1,0 +1,412 @@
+// Persistent grouped FP8 x FP8 GEMM over live row tiles, with the FC1 (SwiGLU + 1x128 requant)
+// and FC2 (BF16 store) epilogues.
+//
+// (vLLM "Skip padded work in block-FP8 DeepGemmExperts", Purpose: both grouped GEMMs visit only
+// the live (expert, row-tile) work named by the prefix-sum endpoints, and the fused activation
+// quantization consumes the same endpoints; SM90 section: whole padded tiles are skipped, padding
+// inside a partially filled tile remains.  TensorRT-LLM "Triton FP8-activation MoE for
+// decode-sized batches on Hopper", human review: per 128-wide K block the partial sum is scaled by
+// the product a_scale*b_scale formed first.)
+//
+// Work item = (live row tile, output column block, K split).  One CTA per SM walks items
+// blockIdx.x, blockIdx.x + gridDim.x, ...; inside the CTA:
+//   warp 0 (one lane)  TMA producer: per 128-wide K block, the tile's live activation rows (32-row
+//                      boxes, only those below the expert's live end) and 256 weight rows, into a
+//                      4-stage ring of 48 KB stages (128-byte swizzle).
+//   warp 1 (one lane)  MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) per K block
+//                      into one of two 256-column fp32 accumulators in tensor memory.
+//   warps 2..9         promotion + epilogue: thread = one workspace row and 128 of the 256 columns;
+//                      per K block it loads its partial sums from tensor memory and accumulates
+//                      acc = fma(partial, a_scale*b_scale, acc) in registers, then releases the
+//                      accumulator buffer so the MMA of the next K block overlaps the promotion.
+// FC1 columns: 128 gate rows of W13 and the matching 128 up rows, so a thread owns 64 (gate, up)
+// pairs of one row and the SwiGLU and 1x128 requantization need only the row amax of the two
+// threads sharing the row.  FC2 columns: 256 consecutive hidden columns, BF16 out.
+// Small batches split K across CTAs (FC1 only): each split writes its fp32 partial rows, the last
+// split to arrive (atomic counter per item) sums the splits in fixed order and runs the epilogue.
+#include "moe_device.cuh"
+
+namespace moe {
+
+constexpr uint32_t kIdesc = make_idesc_e4m3(kBM, kBN);
+
+struct Item {
+  int tile, nb, ks, e, m0, live;
+};
+
+__device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
+  Item it;
+  const int per_tile = p.n_blocks * p.ksplit;
+  it.tile = item / per_tile;
+  const int rem = item - it.tile * per_tile;
+  it.nb = rem / p.ksplit;
+  it.ks = rem - it.nb * p.ksplit;
+  it.e = p.tile_expert[it.tile];
+  it.m0 = it.tile * kBM;
+  it.live = min(kBM, p.live_end[it.e] - it.m0);
+  return it;
+}
+
+// SiLU(g) * u with the optional clamp, fp32, IEEE division, no fused multiply-add.
+__device__ __forceinline__ float swiglu(float g, float u, int mode, float lim) {
+  if (mode == MOE_CLAMP_BEFORE_SILU) {
+    g = fminf(g, lim);
+    u = fminf(fmaxf(u, -lim), lim);
+  }
+  const float sig = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+  float silu = __fmul_rn(g, sig);
+  if (mode == MOE_CLAMP_AFTER_SILU) {
+    silu = fminf(silu, lim);
+    u = fminf(fmaxf(u, -lim), lim);
+  }
+  return __fmul_rn(silu, u);
+}
+
+// Bounded wait used while tearing down: ignores the abort flag.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void promote32(uint32_t taddr, float sab, float* acc) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(r[i]), sab, acc[i]);
+}
+
+template <bool kFC1>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_addr(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_base);
+  uint8_t* ctrl = smem + kStages * kStageBytes;
+  const uint32_t bar0 = smem_addr(ctrl);
+  // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kStages + 5));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* mma_consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  float* red = reinterpret_cast<float*>(ctrl + 1024);   // [2][kBM] row amax of each half
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiThreads / 32);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *mma_consumed = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_tiles = *p.num_tiles;
+  const int total = num_tiles * p.n_blocks * p.ksplit;
+  const int kb_per_split = (p.K / kBK) / p.ksplit;
+  const int KB = p.K / kBK;
+  int* status = p.status;
+
+  int prod_issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    int it = 0;
+    bool ok = true;
+    const uint64_t pol_w = policy_evict_first();
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      const Item w = decode_item(p, item);
+      const int nbox = (w.live + kABoxRows - 1) / kABoxRows;
+      int brow0, brow1;
+      bool second;
+      if (kFC1) {
+        brow0 = w.e * p.b_rows_per_expert + w.nb * kGroup;                  // gate rows
+        brow1 = brow0 + p.out_cols;                                         // matching up rows
+        second = true;
+      } else {
+        brow0 = w.e * p.b_rows_per_expert + w.nb * kBN;
+        brow1 = brow0 + kGroup;
+        second = (w.nb * kBN + kGroup) < p.out_cols;
+      }
+      const uint32_t bytes = nbox * (kABoxRows * kBK) + (second ? 2 : 1) * (kGroup * kBK);
+      const int kb0 = w.ks * kb_per_split;
+      for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(s), bytes);
+        const uint32_t sA = sbase + s * kStageBytes;
+        const uint32_t sB = sA + kABytes;
+        for (int q = 0; q < nbox; ++q)
+          tma_load_2d(sA + q * (kABoxRows * kBK), &tmA, kb * kBK, w.m0 + q * kABoxRows, full_bar(s));
+        tma_load_2d_hint(sB, &tmB, kb * kBK, brow0, full_bar(s), pol_w);
+        if (second) tma_load_2d_hint(sB + kGroup * kBK, &tmB, kb * kBK, brow1, full_bar(s), pol_w);
+        ++it;
+      }
+    }
+    prod_issued = it;
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA
+    int it = 0, c = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      for (int k = 0; k < kb_per_split; ++k) {
+        const int s = it % kStages;
+        const uint32_t ph = (it / kStages) & 1;
+        if (!mbar_wait(full_bar(s), ph, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        const int b = c & 1;
+        const uint32_t tph = (c >> 1) & 1;
+        if (!mbar_wait(tempty_bar(b), tph ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t d = tmem_base + b * kBN;
+        const uint32_t sA = sbase + s * kStageBytes;
+        const uint64_t adesc = make_sdesc_sw128(sA);
+        const uint64_t bdesc = make_sdesc_sw128(sA + kABytes);
+#pragma unroll
+        for (int kk = 0; kk < kBK / 32; ++kk)
+          mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+        mma_commit(empty_bar(s));
+        mma_commit(tfull_bar(b));
+        ++it;
+        ++c;
+        *mma_consumed = it;
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ---------------------------------------------------- promotion + epilogue
+    const int ew = warp - kEpiWarp0;
+    const int wg = ew >> 2;          // which half of the 256 columns
+    const int q = warp & 3;          // TMEM lane quarter this warp may access
+    const int row = q * 32 + lane;   // row inside the tile
+    const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
+    const int ncb = p.b_rows_per_expert / kGroup;   // weight row blocks per expert
+    int c = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      const Item w = decode_item(p, item);
+      const bool qlive = q * 32 < w.live;
+      const bool rlive = row < w.live;
+      float acc[128];
+#pragma unroll
+      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+      const int kb0 = w.ks * kb_per_split;
+      for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
+        const int b = c & 1;
+        const uint32_t ph = (c >> 1) & 1;
+        float sa = 0.0f, sw0 = 0.0f, sw1 = 0.0f;
+        if (qlive) {
+          sa = load_scale(p.a_scale, (size_t)kb * p.R_cap + w.m0 + row, a_ue);
+          if (kFC1) {
+            sw0 = load_scale(p.b_scale, ((size_t)w.e * ncb + w.nb) * KB + kb, b_ue);
+            sw1 = load_scale(p.b_scale, ((size_t)w.e * ncb + p.out_cols / kGroup + w.nb) * KB + kb, b_ue);
+          } else {
+            const int hb = w.nb * 2 + wg;
+            sw0 = hb < ncb ? load_scale(p.b_scale, ((size_t)w.e * ncb + hb) * KB + kb, b_ue) : 0.0f;
+          }
+        }
+        if (!mbar_wait(tfull_bar(b), ph, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (qlive) {
+          const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
+          if (kFC1) {
+            const float sg = __fmul_rn(sa, sw0), su = __fmul_rn(sa, sw1);
+            promote32(t0 + wg * 64, sg, acc);
+            promote32(t0 + wg * 64 + 32, sg, acc + 32);
+            promote32(t0 + kGroup + wg * 64, su, acc + 64);
+            promote32(t0 + kGroup + wg * 64 + 32, su, acc + 96);
+          } else {
+            const float s = __fmul_rn(sa, sw0);
+            promote32(t0 + wg * 128, s, acc);
+            promote32(t0 + wg * 128 + 32, s, acc + 32);
+            promote32(t0 + wg * 128 + 64, s, acc + 64);
+            promote32(t0 + wg * 128 + 96, s, acc + 96);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar(b));
+        ++c;
+      }
+      if (!ok) break;
+
+      if (kFC1) {
+        const int I = p.out_cols;
+        if (p.ksplit > 1) {
+          // split-K fix-up: publish this split's partial rows, the last split sums all of them
+          const int pair = rlive ? p.sorted_pair[w.m0 + row] : 0;
+          if (rlive) {
+            float* dst = p.splitk_partial + ((size_t)w.ks * p.P_cap + pair) * (2 * I);
+#pragma unroll
+            for (int i = 0; i < 64; i += 4) {
+              *reinterpret_cast<float4*>(dst + w.nb * kGroup + wg * 64 + i) =
+                  make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
+              *reinterpret_cast<float4*>(dst + I + w.nb * kGroup + wg * 64 + i) =
+                  make_float4(acc[64 + i], acc[65 + i], acc[66 + i], acc[67 + i]);
+            }
+          }
+          __threadfence();
+          named_barrier_sync(1, kEpiThreads);
+          if (ew == 0 && lane == 0) {
+            const int prev = atomicAdd(&p.splitk_count[w.tile * p.n_blocks + w.nb], 1);
+            *last_flag = (prev == p.ksplit - 1);
+          }
+          named_barrier_sync(1, kEpiThreads);
+          const bool last = *last_flag != 0;
+          named_barrier_sync(1, kEpiThreads);
+          if (!last) continue;
+          __threadfence();
+          if (ew == 0 && lane == 0) p.splitk_count[w.tile * p.n_blocks + w.nb] = 0;
+          if (rlive) {
+#pragma unroll
+            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
+            for (int s = 0; s < p.ksplit; ++s) {
+              const float* src = p.splitk_partial + ((size_t)s * p.P_cap + pair) * (2 * I);
+#pragma unroll
+              for (int i = 0; i < 64; i += 4) {
+                const float4 g = __ldcg(reinterpret_cast<const float4*>(src + w.nb * kGroup + wg * 64 + i));
+                const float4 u = __ldcg(reinterpret_cast<const float4*>(src + I + w.nb * kGroup + wg * 64 + i));
+                acc[i] = __fadd_rn(acc[i], g.x);
+                acc[i + 1] = __fadd_rn(acc[i + 1], g.y);
+                acc[i + 2] = __fadd_rn(acc[i + 2], g.z);
+                acc[i + 3] = __fadd_rn(acc[i + 3], g.w);
+                acc[64 + i] = __fadd_rn(acc[64 + i], u.x);
+                acc[65 + i] = __fadd_rn(acc[65 + i], u.y);
+                acc[66 + i] = __fadd_rn(acc[66 + i], u.z);
+                acc[67 + i] = __fadd_rn(acc[67 + i], u.w);
+              }
+            }
+          }
+        }
+        // SwiGLU on the BF16-rounded FC1 outputs, then 1x128 requantization over the row's 128
+        // (gate, up) columns held by this thread (64) and its partner in the other half (64).
+        float amax = 0.0f;
+        if (rlive) {
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            const float h = swiglu(bf16_round(acc[i]), bf16_round(acc[64 + i]), p.clamp_mode,
+                                   p.clamp_limit);
+            acc[i] = h;
+            amax = fmaxf(amax, fabsf(h));
+          }
+        }
+        red[wg * kBM + row] = amax;
+        named_barrier_sync(1, kEpiThreads);
+        amax = fmaxf(red[row], red[kBM + row]);
+        named_barrier_sync(1, kEpiThreads);
+        if (rlive) {
+          const float s = group_scale(amax, p.act_fmt);
+          uint8_t* dst = p.a2_q + (size_t)(w.m0 + row) * I + w.nb * kGroup + wg * 64;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            uint32_t wd[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+              const float* h = acc + v * 16 + j * 4;
+              wd[j] = cvt_e4m3x2(__fdiv_rn(h[0], s), __fdiv_rn(h[1], s)) |
+                      (cvt_e4m3x2(__fdiv_rn(h[2], s), __fdiv_rn(h[3], s)) << 16);
+            }
+            *reinterpret_cast<uint4*>(dst + v * 16) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          }
+          if (wg == 0)
+            store_scale(p.a2_s, (size_t)w.nb * p.R_cap + w.m0 + row, s, p.act_fmt == MOE_SCALE_UE8M0);
+        }
+      } else {
+        const int col0 = w.nb * kBN + wg * kGroup;
+        if (rlive && col0 < p.out_cols) {
+          uint16_t* dst = p.y + (size_t)(w.m0 + row) * p.out_cols + col0;
+#pragma unroll
+          for (int v = 0; v < 16; ++v) {
+            uint32_t wd[4];
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              wd[j] = f32_to_bf16_bits(acc[v * 8 + 2 * j]) |
+                      (f32_to_bf16_bits(acc[v * 8 + 2 * j + 1]) << 16);
+            *reinterpret_cast<uint4*>(dst + v * 8) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (warp == 1 && lane == 0) {
+    // every MMA this CTA issued has completed (and its barrier arrivals have landed)
+    mma_commit(drain_bar);
+    drain_wait(drain_bar, 0, status);
+  }
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    // loads issued but never consumed are still in flight: wait for them before leaving
+    for (int it = *mma_consumed; it < prod_issued; ++it)
+      drain_wait(full_bar(it % kStages), (it / kStages) & 1, status);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kTmemCols);
+  }
+}
+
+template <bool kFC1>
+static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                               int grid, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<kFC1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+  if (err != cudaSuccess) return err;
+  k_grouped_gemm<kFC1><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(tmA, tmB, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                       int grid, cudaStream_t s) {
+  return launch_gemm<true>(tmA, tmB, p, grid, s);
+}
+
+cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                       int grid, cudaStream_t s) {
+  return launch_gemm<false>(tmA, tmB, p, grid, s);
+}
+
+}  // namespace moe

@@ -1,0 +1,120 @@
+// Internal declarations shared by the library's translation units: constants, the kernel
+// parameter blocks and the launchers each .cu file provides.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe_fp8.h"
+
+namespace moe {
+
+constexpr int kAlign = 128;               // expert segment alignment = GEMM row-tile height
+constexpr int kGroup = 128;               // 1x128 activation group = 128x128 weight block
+constexpr int kMaxExperts = 1024;
+constexpr int kMaxTopk = 16;
+constexpr int kMaxPairs = 1 << 20;
+constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s bound on any device-side wait
+constexpr float kScaleFloor = 1.0f / 229376.0f;    // 1/(448*512), rounded to fp32
+
+// ---------------------------------------------------------------- GEMM tiling
+// One CTA tile: 128 workspace rows (the MMA's M) x 256 weight rows (the MMA's N) x 128 of K per
+// stage.  FC1: the 256 weight rows are 128 gate rows and the matching 128 up rows.
+constexpr int kBM = 128;
+constexpr int kBN = 256;
+constexpr int kBK = 128;
+constexpr int kStages = 4;
+constexpr int kABoxRows = 32;                         // activation rows per TMA box
+constexpr int kABytes = kBM * kBK;                    // 16 KB
+constexpr int kBBytes = kBN * kBK;                    // 32 KB
+constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kGemmThreads = 320;                     // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kEpiWarp0 = 2;
+constexpr int kEpiThreads = 256;
+constexpr int kTmemCols = 512;                        // two 256-column accumulators
+constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 1024 /*bars*/ +
+                               2 * kBM * 4 /*row amax exchange*/;
+
+struct Plan {
+  moe_ws_plan ws;
+  int M_cap, E, H, I, topk;
+  int act_fmt;
+};
+
+moe_status make_plan(int M_cap, int E, int H, int I, int topk, int act_fmt, Plan* plan);
+
+// ------------------------------------------------------------ kernel params
+struct AlignParams {
+  const int32_t* topk_ids;
+  const int32_t* d_num_tokens;
+  int M_cap, topk, E;
+  int32_t* seg_start;
+  int32_t* live_end;
+  int32_t* sorted_pair;
+  int32_t* pair_row;
+  int32_t* tile_expert;
+  int32_t* num_tiles;
+  int32_t* status;
+  int32_t* splitk_count;
+  int splitk_count_len;
+};
+
+struct QuantParams {
+  const uint16_t* x;
+  const int32_t* d_num_tokens;
+  const int32_t* pair_row;
+  int M_cap, H, topk, R_cap;
+  int fmt;
+  uint8_t* a_q;
+  void* a_s;
+};
+
+struct GemmParams {
+  const int32_t* tile_expert;
+  const int32_t* num_tiles;
+  const int32_t* live_end;
+  const void* a_scale;      // column-major [K/128][R_cap]
+  int a_scale_ue8m0;
+  const void* b_scale;      // [E][Nrows/128][K/128]
+  int b_scale_ue8m0;
+  int K;                    // reduction length (H for FC1, I for FC2)
+  int R_cap;
+  int n_blocks;             // output column blocks per tile (I/128 for FC1, ceil(H/256) for FC2)
+  int b_rows_per_expert;    // 2I for FC1, H for FC2
+  int out_cols;             // I for FC1 (a2_q row length), H for FC2 (y row length)
+  int ksplit;               // FC1 K-split factor
+  // FC1 epilogue
+  uint8_t* a2_q;
+  void* a2_s;
+  int act_fmt;
+  int clamp_mode;
+  float clamp_limit;
+  float* splitk_partial;    // [ksplit][P_cap][2I] fp32
+  int32_t* splitk_count;    // [T_cap * n_blocks]
+  const int32_t* sorted_pair;
+  int P_cap;
+  // FC2 epilogue
+  uint16_t* y;
+  int32_t* status;
+};
+
+struct ReduceParams {
+  const uint16_t* y;
+  const int32_t* pair_row;
+  const float* topk_weights;
+  const int32_t* d_num_tokens;
+  int M_cap, H, topk;
+  uint16_t* out;
+};
+
+cudaError_t launch_align(const AlignParams& p, cudaStream_t s);
+cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
+cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                       int grid, cudaStream_t s);
+cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
+                       int grid, cudaStream_t s);
+cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t s);
+
+}  // namespace moe

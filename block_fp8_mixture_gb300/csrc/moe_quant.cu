@@ -1,0 +1,108 @@
+// Per-1x128 activation quantization scattered into the aligned workspace, and the top-k weighted
+// unpermute/sum.  Both are HBM-bound streaming kernels: 16-byte vector loads and stores, one
+// half-warp per 128-element group, and grids that only do work for live tokens.
+#include "moe_device.cuh"
+
+namespace moe {
+
+// ------------------------------------------------------------ quantization
+// (vLLM "per-layer activation scale format + fused SiLU+quant", Details: scale =
+// max(amax/448, 1/(448*512)) then x/scale; TensorRT-LLM "Triton FP8-activation MoE for
+// decode-sized batches on Hopper", rounding-fix commit: correctly rounded division.)
+// One half-warp quantizes one 1x128 group: each lane holds 8 BF16 values (one 16-byte load),
+// the group amax is reduced with shuffles inside the half-warp, and the 8 codes (8 bytes) plus the
+// scale are written to every live workspace row of the token.
+constexpr int kQuantThreads = 256;
+constexpr int kGroupsPerBlock = kQuantThreads / 16;
+
+__global__ void __launch_bounds__(kQuantThreads) k_quant_act(QuantParams p) {
+  const int groups_per_row = p.H / kGroup;
+  const int half = (threadIdx.x >> 4) & 1;
+  const int l16 = threadIdx.x & 15;
+  const uint32_t hmask = 0xFFFFu << (16 * half);
+  const long gid = (long)blockIdx.x * kGroupsPerBlock + (threadIdx.x >> 4);
+  const long t = gid / groups_per_row;
+  const int g = (int)(gid % groups_per_row);
+  int n = p.M_cap;
+  if (p.d_num_tokens != nullptr) n = min(max(*p.d_num_tokens, 0), p.M_cap);
+  if (t >= n) return;   // the whole half-warp leaves together
+
+  const uint4 raw = *reinterpret_cast<const uint4*>(p.x + t * p.H + g * kGroup + l16 * 8);
+  float v[8];
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+    v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, d));
+  const float s = group_scale(amax, p.fmt);
+  uint32_t q0 = cvt_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
+                (cvt_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
+  uint32_t q1 = cvt_e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) |
+                (cvt_e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
+  const int is_ue8m0 = p.fmt == MOE_SCALE_UE8M0;
+  for (int j = 0; j < p.topk; ++j) {
+    const int row = p.pair_row[t * p.topk + j];
+    if (row < 0) continue;
+    *reinterpret_cast<uint2*>(p.a_q + (size_t)row * p.H + g * kGroup + l16 * 8) = make_uint2(q0, q1);
+    if (l16 == 0) store_scale(p.a_s, (size_t)g * p.R_cap + row, s, is_ue8m0);
+  }
+}
+
+cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
+  const long groups = (long)p.M_cap * (p.H / kGroup);
+  const long blocks = (groups + kGroupsPerBlock - 1) / kGroupsPerBlock;
+  if (blocks == 0) return cudaSuccess;
+  k_quant_act<<<(unsigned)blocks, kQuantThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+// ----------------------------------------------------------------- reduce
+// (TensorRT-LLM page, rounding-fix commit: the routing weights scale the BF16 expert outputs in
+// fp32 in the top-k sum, not the FC2 accumulators.)
+// out[t, c] = bf16( sum_j RN(RN(w[t,j] * y[row_j, c]) ) ) over pairs j with a row, j ascending.
+// Each thread produces 8 consecutive columns (16-byte loads of y and a 16-byte store).
+constexpr int kReduceThreads = 128;
+
+__global__ void __launch_bounds__(kReduceThreads) k_topk_reduce(ReduceParams p) {
+  const long t = blockIdx.x;
+  int n = p.M_cap;
+  if (p.d_num_tokens != nullptr) n = min(max(*p.d_num_tokens, 0), p.M_cap);
+  if (t >= n) return;
+  const int c0 = (blockIdx.y * kReduceThreads + threadIdx.x) * 8;
+  if (c0 >= p.H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int j = 0; j < p.topk; ++j) {
+    const int row = p.pair_row[t * p.topk + j];
+    if (row < 0) continue;
+    const float w = p.topk_weights[t * p.topk + j];
+    const uint4 raw = *reinterpret_cast<const uint4*>(p.y + (size_t)row * p.H + c0);
+    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, bf16_bits_to_f32(u[i] & 0xFFFFu)));
+      acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, bf16_bits_to_f32(u[i] >> 16)));
+    }
+  }
+  uint32_t o[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i)
+    o[i] = f32_to_bf16_bits(acc[2 * i]) | (f32_to_bf16_bits(acc[2 * i + 1]) << 16);
+  *reinterpret_cast<uint4*>(p.out + t * p.H + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t s) {
+  if (p.M_cap == 0) return cudaSuccess;
+  dim3 grid(p.M_cap, (p.H / 8 + kReduceThreads - 1) / kReduceThreads);
+  k_topk_reduce<<<grid, kReduceThreads, 0, s>>>(p);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,181 @@
+/*
+ * moe_fp8.h -- C ABI of the block-FP8 mixture-of-experts layer forward on one GB300 (sm_103a).
+ *
+ * The layer (composite of three pages on the subject):
+ *   routing alignment into per-expert prefix-sum endpoints
+ *     (vLLM "Skip padded work in block-FP8 DeepGemmExperts", Purpose;
+ *      TensorRT-LLM "Triton FP8-activation MoE for decode-sized batches on Hopper", description)
+ *   -> per-1x128 FP8 E4M3 activation quantization
+ *     (TensorRT-LLM page, description; vLLM "per-layer activation scale format + fused SiLU+quant", Details)
+ *   -> FC1 (gate+up) grouped FP8 x FP8 GEMM with 128x128 weight block scales
+ *   -> SwiGLU (optionally clamped) fused with the 1x128 requantization of the FC2 input
+ *   -> FC2 grouped GEMM, BF16 per-pair output
+ *   -> routing-weighted top-k unpermute/sum (TensorRT-LLM page, rounding-fix commit).
+ *
+ * Conventions (every entry point):
+ *   - All tensor arguments are DEVICE pointers owned by the caller. The library allocates no
+ *     memory, never synchronizes the host (except moe_last_device_status), and issues all work on
+ *     the given stream, so a whole forward can be captured in a CUDA graph.
+ *   - Arguments are validated on the host before anything is launched; a failed check returns a
+ *     status and launches nothing.  A CUDA launch error returns MOE_ERR_CUDA.
+ *   - Row-major layouts; "K-major" weights store each output row's K values contiguously.
+ *   - Token count: d_num_tokens, when not NULL, is a device int32 holding the number of live tokens
+ *     n (clamped to [0, M_cap]); rows t >= n of x, topk_ids and topk_weights are never read and rows
+ *     t >= n of out are never written (vLLM padded-work page, SM100 section: GPU token-count
+ *     metadata).  NULL means n = M_cap.
+ *   - Expert ids outside [0, E) (including -1) are dropped: such pairs get no workspace row and add
+ *     nothing to the output.
+ *   - Workspace rows outside the live part of each expert segment are never written.
+ *   - Every device-side wait is bounded; on expiry the kernel records MOE_ERR_DEVICE_TIMEOUT in the
+ *     workspace status word and exits (read it with moe_last_device_status).
+ *
+ * Shapes: E experts, H hidden, I intermediate per expert, k = topk, M_cap token capacity,
+ * P_cap = M_cap * k pairs, R_cap workspace rows (moe_ws_plan.R_cap).
+ * Supported: H % 128 == 0, I % 128 == 0, 128 <= H <= 32768, 128 <= I <= 16384, 1 <= k <= 16,
+ * 1 <= E <= 1024, 0 <= M_cap, M_cap * k <= 2^20.  Pointers: 16-byte aligned; workspace 256-byte aligned.
+ */
+#ifndef MOE_FP8_H_
+#define MOE_FP8_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* same type as cudaStream_t; NULL = legacy default stream */
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,         /* NULL or misaligned pointer, bad enum, negative size */
+  MOE_ERR_UNSUPPORTED_SHAPE = 2,   /* shape outside the supported set above */
+  MOE_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < moe_workspace_bytes(...) */
+  MOE_ERR_CUDA = 4,                /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5       /* a bounded device-side wait expired (read from the workspace) */
+} moe_status;
+
+/* Scale formats (vLLM per-layer scale page, Overview and Details; vLLM padded-work page, Purpose):
+ * FP32      -- fp32 scales, amax/448 (floored at 1/(448*512)).
+ * FP32_POW2 -- fp32 scales rounded up to a power of two.
+ * UE8M0     -- one byte b per scale, value 2^(b-127) (power of two, rounded up).
+ * Weight scales are either FP32 (FP32_POW2 stores the same way) or UE8M0 bytes. */
+typedef enum { MOE_SCALE_FP32 = 0, MOE_SCALE_FP32_POW2 = 1, MOE_SCALE_UE8M0 = 2 } moe_scale_fmt;
+
+/* SwiGLU clamp (TensorRT-LLM page, test coverage: no clamp, clamp, clamp after SiLU):
+ * BEFORE_SILU: gate <- min(gate, L), up <- clamp(up, -L, L), then SiLU(gate) * up.
+ * AFTER_SILU:  min(SiLU(gate), L) * clamp(up, -L, L). */
+typedef enum { MOE_CLAMP_NONE = 0, MOE_CLAMP_BEFORE_SILU = 1, MOE_CLAMP_AFTER_SILU = 2 } moe_clamp_mode;
+
+/* Byte offsets of the workspace sub-buffers (all 256-byte aligned) and derived sizes.
+ * Layout of each sub-buffer:
+ *   status       int32        device status word (0 = ok, else a moe_status)
+ *   num_tiles    int32        number of live 128-row tiles
+ *   seg_start    int32[E+1]   expert segment starts (multiples of 128); seg_start[E] = rows used
+ *   live_end     int32[E]     seg_start[e] + count of expert e
+ *   sorted_pair  int32[R_cap] pair index p = t*k + j of each live row (padding rows not written)
+ *   pair_row     int32[P_cap] workspace row of each pair p < n*k, -1 when dropped
+ *   tile_expert  int32[T_cap] expert of row tile i (rows [128 i, 128 i + 128)), i < num_tiles
+ *   a1_q         uint8[R_cap][H]       FC1 input, E4M3 codes
+ *   a1_s         [H/128][R_cap]        FC1 input scales, column-major (fp32, or uint8 for UE8M0)
+ *   a2_q         uint8[R_cap][I]       FC2 input, E4M3 codes
+ *   a2_s         [I/128][R_cap]        FC2 input scales, column-major (fp32 or uint8)
+ *   y            bf16[R_cap][H]        FC2 output per pair row (routing weights not applied)
+ *   splitk       fp32 partial sums and int32 tile counters of the split-K FC1 schedule */
+typedef struct {
+  size_t status, num_tiles, seg_start, live_end, sorted_pair, pair_row, tile_expert;
+  size_t a1_q, a1_s, a2_q, a2_s, y, splitk_partial, splitk_count;
+  size_t total_bytes;
+  int32_t R_cap;   /* workspace rows: roundup(P_cap + min(E, P_cap) * 127, 128) */
+  int32_t T_cap;   /* R_cap / 128 */
+  int32_t P_cap;   /* M_cap * k */
+  int32_t fc1_ksplit; /* K-split factor the forward uses for FC1 (1 = none) */
+} moe_ws_plan;
+
+/* Workspace plan for a layer shape; returns MOE_OK or a validation status. */
+moe_status moe_workspace_plan(int M_cap, int E, int H, int I, int topk, moe_scale_fmt act_fmt,
+                              moe_ws_plan* plan);
+
+/* Bytes of workspace moe_fp8_block_forward needs (0 if the shape is unsupported). */
+size_t moe_workspace_bytes(int M_cap, int E, int H, int I, int topk, moe_scale_fmt act_fmt);
+
+/* Routing alignment (vLLM padded-work page, Purpose: "the shared permutation helper produces expert
+ * endpoints"; TensorRT-LLM page: single-program moe_align).
+ * Stable counting sort of the valid pairs p = t*k + j (t < n) by expert; expert e's segment starts at
+ * seg_start[e] (exclusive prefix sum of counts rounded up to 128) and its live rows end at
+ * live_end[e]; inside a segment pairs keep ascending p.  Writes, for p < n*k, pair_row[p] (row or -1)
+ * and, for live rows, sorted_pair[row] = p; tile_expert[i] for every 128-row tile i < num_tiles.
+ * Also resets the workspace status word.  Runs as one CTA.
+ * topk_ids: int32 [M_cap, topk]; all outputs are sub-buffers of the workspace of the same plan. */
+moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M_cap, int topk, int E,
+                     int H, int I, moe_scale_fmt act_fmt, void* workspace, size_t workspace_bytes,
+                     moe_stream_t stream);
+
+/* Per-1x128 activation quantization scattered to the aligned workspace (vLLM per-layer scale page,
+ * Details: scale = max(amax/448, 1/(448*512)), codes = RNE_satfinite(x/scale) with IEEE division;
+ * power-of-two formats round the scale up).  For each live token t < n and 128-group g of H, the
+ * codes go to a1_q[row][g*128 ...] and the scale to a1_s[g][row] for every row = pair_row[t*k+j] >= 0.
+ * x: bf16 [M_cap, H].  Requires moe_align on the same workspace first (same stream). */
+moe_status moe_quant_act(const void* x_bf16, const int32_t* d_num_tokens, int M_cap, int E, int H,
+                         int I, int topk, moe_scale_fmt act_fmt, void* workspace,
+                         size_t workspace_bytes, moe_stream_t stream);
+
+/* Problem statement of one layer call. */
+typedef struct {
+  const void* x;               /* bf16 [M_cap, H] */
+  const int32_t* topk_ids;     /* int32 [M_cap, topk] */
+  const float* topk_weights;   /* fp32 [M_cap, topk] */
+  const int32_t* d_num_tokens; /* device int32 n, or NULL for n = M_cap */
+  const void* w13;             /* E4M3 [E, 2I, H]: rows [0, I) gate, [I, 2I) up, K-major */
+  const void* s13;             /* [E, 2I/128, H/128] fp32, or uint8 UE8M0 */
+  const void* w2;              /* E4M3 [E, H, I], K-major */
+  const void* s2;              /* [E, H/128, I/128] fp32, or uint8 UE8M0 */
+  void* out;                   /* bf16 [M_cap, H]; rows t >= n untouched */
+  int M_cap, E, H, I, topk;
+  moe_scale_fmt weight_scale_fmt; /* FP32 (or FP32_POW2, same storage) or UE8M0 */
+  moe_scale_fmt act_scale_fmt;    /* FP32, FP32_POW2 or UE8M0 */
+  moe_clamp_mode clamp_mode;
+  float clamp_limit;              /* L >= 0 when clamp_mode != NONE */
+} moe_fwd_args;
+
+/* FC1 grouped GEMM over live 128-row tiles with the SwiGLU + 1x128 requantization epilogue
+ * (vLLM padded-work page, Purpose: the prefix-sum scheduler visits only live tiles and the fused
+ * activation quantization consumes the same endpoints; TensorRT-LLM page, human review: the scale
+ * product a_scale*b_scale is formed before it multiplies the partial sum).
+ * For each live row r of expert e and output column c:
+ *   acc = sum over 128-wide K blocks kb of  p_kb * (a1_s[kb][r] * s13[e][c/128][kb])
+ * with p_kb the FP8 dot of the block in fp32; g1 = bf16(acc); h = SwiGLU(gate, up) in fp32 with the
+ * clamp; then a2_q / a2_s = 1x128 quantization of h.  Reads a1_q/a1_s, writes a2_q/a2_s.
+ * Uses args->w13, s13, M_cap, E, H, I, topk, formats, clamp. */
+moe_status moe_fc1_swiglu_quant(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                                moe_stream_t stream);
+
+/* FC2 grouped GEMM over live tiles: y[r][c] = bf16(sum_kb p_kb * (a2_s[kb][r] * s2[e][c/128][kb])).
+ * Routing weights are not applied here (TensorRT-LLM page, rounding-fix commit). */
+moe_status moe_fc2(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                   moe_stream_t stream);
+
+/* Top-k weighted unpermute/sum: out[t] = bf16( sum_j fp32(w[t,j] * y[pair_row[t*k+j]]) ), j ascending,
+ * fp32 multiply and add rounded separately, dropped pairs skipped; rows t < n only. */
+moe_status moe_topk_reduce(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream);
+
+/* The whole layer: moe_align -> moe_quant_act -> moe_fc1_swiglu_quant -> moe_fc2 -> moe_topk_reduce,
+ * all on `stream`, no host synchronization. */
+moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream);
+
+/* Reads the workspace status word (synchronizes `stream` first).  MOE_OK or MOE_ERR_DEVICE_TIMEOUT. */
+moe_status moe_last_device_status(const void* workspace, moe_stream_t stream);
+
+/* Human-readable name of a status. */
+const char* moe_status_str(moe_status status);
+
+/* Library version string. */
+const char* moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_FP8_H_ */

@@ -1,0 +1,236 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the same seeded inputs.
+
+Bars: alignment arrays and FC1-input codes/scales bit-exact; layer outputs within
+1e-2 * max|oracle| per element; >= 99.9% of FC2-input codes identical; padded workspace rows and
+output rows t >= n untouched.
+"""
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from moe_testutil import (CODE_MATCH_MIN, assert_layer_close, bf16_tensor_to_f32, check_a2_codes,
+                          check_untouched, device_case, oracle_forward, run_forward, scale_values)
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+if not torch.cuda.is_available():
+    pytest.skip("no CUDA device", allow_module_level=True)
+
+import block_fp8_mixture_gb300 as moe  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    moe.load_library(build_if_missing=True)
+
+
+# ------------------------------------------------------------------ align
+ALIGN_CASES = [
+    # (E, topk, M_cap, n, id_low, id_high)
+    (8, 2, 16, 16, 0, 8),
+    (72, 8, 16, 16, 0, 72),       # 128-pair threshold, non-power-of-two expert count
+    (72, 8, 24, 24, 0, 72),       # above it
+    (288, 8, 32, 32, -1, 290),    # invalid ids dropped
+    (32, 8, 512, 16, 0, 32),      # device token count below capacity
+    (128, 8, 8192, 8192, 0, 128),
+    (1024, 4, 300, 257, -3, 1030),
+    (5, 3, 0, 0, 0, 5),           # no tokens
+    (16, 1, 64, 0, 0, 16),        # capacity but zero live tokens
+]
+
+
+@pytest.mark.parametrize("E,topk,M_cap,n,lo,hi", ALIGN_CASES)
+def test_align_bit_exact(E, topk, M_cap, n, lo, hi):
+    rng = np.random.default_rng(E * 1000 + M_cap)
+    ids = rng.integers(lo, hi, (M_cap, topk)).astype(np.int32)
+    H, I = 256, 256
+    ws = moe.alloc_workspace(M_cap, E, H, I, topk)
+    ws.fill_(0xFF)
+    d_ids = torch.from_numpy(ids).cuda()
+    d_n = torch.tensor([n], dtype=torch.int32, device="cuda")
+    moe.align(d_ids, E, H, I, ws, d_num_tokens=d_n)
+    torch.cuda.synchronize()
+    v = moe.workspace_views(ws, M_cap, E, H, I, topk)
+    ref = oracle.align(ids, n, E)
+    assert np.array_equal(v["seg_start"].cpu().numpy(), ref["seg_start"])
+    assert np.array_equal(v["live_end"].cpu().numpy(), ref["live_end"])
+    assert int(v["num_tiles"].item()) == ref["num_tiles"]
+    assert np.array_equal(v["pair_row"].cpu().numpy()[: n * topk], ref["pair_row"])
+    nt = ref["num_tiles"]
+    assert np.array_equal(v["tile_expert"].cpu().numpy()[:nt], ref["tile_expert"])
+    sp = v["sorted_pair"].cpu().numpy()
+    live = ref["sorted_pair"] >= 0
+    assert np.array_equal(sp[: live.size][live], ref["sorted_pair"][live])
+    assert moe.last_device_status(ws) == moe.MOE_OK
+
+
+# ------------------------------------------------------------------ quant
+@pytest.mark.parametrize("fmt", [moe.SCALE_FP32, moe.SCALE_FP32_POW2, moe.SCALE_UE8M0])
+@pytest.mark.parametrize("H,M_cap,n,outliers", [(512, 16, 16, 0.0), (7168, 64, 40, 0.0),
+                                                (2048, 300, 300, 0.01), (4096, 3, 1, 0.0)])
+def test_quant_bit_exact(fmt, H, M_cap, n, outliers):
+    E, topk, I = 16, 4, 256
+    rng = np.random.default_rng(H + M_cap + fmt)
+    x = rng.standard_normal((M_cap, H)).astype(np.float32)
+    if outliers:
+        x = np.where(rng.uniform(size=x.shape) < outliers, x * 10, x).astype(np.float32)
+    x[0, :128] = 0.0                       # an all-zero group hits the scale floor
+    x[min(1, M_cap - 1), 128:256] *= 1e-6  # tiny group
+    xt = torch.from_numpy(x).to(torch.bfloat16)
+    x_f = xt.float().numpy()
+    ids = np.stack([rng.permutation(E)[:topk] for _ in range(M_cap)]).astype(np.int32)
+    ids[0, 0] = -1
+    ws = moe.alloc_workspace(M_cap, E, H, I, topk, fmt)
+    ws.fill_(0xFF)
+    d_n = torch.tensor([n], dtype=torch.int32, device="cuda")
+    moe.align(torch.from_numpy(ids).cuda(), E, H, I, ws, d_num_tokens=d_n, act_fmt=fmt)
+    moe.quant_act(xt.cuda(), topk, E, I, ws, d_num_tokens=d_n, act_fmt=fmt)
+    torch.cuda.synchronize()
+    v = moe.workspace_views(ws, M_cap, E, H, I, topk, fmt)
+    pair_row = v["pair_row"].cpu().numpy()
+    a1q = v["a1_q"].cpu().numpy()
+    a1s = v["a1_s"].cpu().numpy()
+    q_ref, s_ref = oracle.quant_1x128(x_f[:n], fmt)
+    for t in range(n):
+        for j in range(topk):
+            row = pair_row[t * topk + j]
+            if ids[t, j] < 0:
+                assert row == -1
+                continue
+            assert np.array_equal(a1q[row], q_ref[t]), (t, j)
+            got_s = a1s[:, row]
+            if fmt == moe.SCALE_UE8M0:
+                assert np.array_equal(got_s, oracle.scale_bytes(s_ref[t]))
+            else:
+                assert np.array_equal(got_s.view(np.uint32), s_ref[t].view(np.uint32))
+
+
+# ------------------------------------------------------------------ layer
+def _layer_check(case, *, tokens=None, check_codes=True, check_poison=True):
+    out, ws, views = run_forward(case)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    gpu = bf16_tensor_to_f32(out)
+    sel = np.arange(case.n) if tokens is None else np.asarray(tokens)
+    ref, pairs = oracle_forward(case, sel, return_pairs=True)
+    rel = assert_layer_close(gpu[sel], ref, case.shape.name)
+    if check_codes and pairs:
+        share = check_a2_codes(case, views, pairs)
+        assert share >= 0.999, share
+    if check_poison:
+        if case.n < case.M_cap:
+            assert bool((out[case.n:].view(torch.int16) == -1).all()), "rows t >= n written"
+        check_untouched(case, views)
+    return rel, out
+
+
+def test_layer_tiny():
+    _layer_check(synth.make_case("tiny", 16))
+
+
+@pytest.mark.parametrize("clamp_mode,limit", [(0, 0.0), (1, 0.02), (2, 0.01)])
+@pytest.mark.parametrize("act_fmt", [0, 1, 2])
+def test_layer_small_variants(clamp_mode, limit, act_fmt):
+    shape = synth.small_shape("small_v", E=12, H=512, I=384, topk=3, act_fmt=act_fmt,
+                              clamp_mode=clamp_mode, limit=limit)
+    _layer_check(synth.make_case("small_v", 40, 33, shape=shape))
+
+
+def test_layer_small_ue8m0_weights():
+    shape = synth.small_shape("small_u", E=10, H=1024, I=256, topk=4, act_fmt=2, weight_fmt=2)
+    _layer_check(synth.make_case("small_u", 64, shape=shape))
+
+
+@pytest.mark.parametrize("M", [1, 4, 32])
+def test_layer_decode(M):
+    _layer_check(synth.make_case("decode", M))
+
+
+def test_layer_padded_16_live():
+    _layer_check(synth.make_case("padded", 512, 16))
+
+
+def test_layer_empty_and_dropped():
+    shape = synth.small_shape("small_e", E=8, H=256, I=256, topk=2)
+    case = synth.make_case("small_e", 20, shape=shape)
+    case.topk_ids[:] = -1
+    case.topk_ids[3, 1] = 5           # a single live pair
+    _layer_check(case)
+    zero = synth.make_case("small_e", 20, 0, shape=shape)
+    out, ws, views = run_forward(zero)
+    torch.cuda.synchronize()
+    assert bool((out.view(torch.int16) == -1).all())
+
+
+@pytest.mark.parametrize("name,M", [("glm_slice", 64), ("mid", 128)])
+def test_layer_mid_sizes_full(name, M):
+    _layer_check(synth.make_case(name, M))
+
+
+@pytest.mark.parametrize("name,M_cap,n", [("padded", 4096, 4096), ("glm_slice", 4096, 4096),
+                                          ("mid", 8192, 8192), ("glm_slice", 1024, 1024),
+                                          ("mid", 2048, 2048)])
+def test_layer_large_sampled(name, M_cap, n):
+    case = synth.make_case(name, M_cap, n)
+    tokens = np.random.default_rng(M_cap).choice(n, 6, replace=False)
+    _layer_check(case, tokens=tokens)
+
+
+def test_layer_forced_empty_experts():
+    case = synth.make_case("mid", 512, routing="softmax_empty4")
+    assert not np.any(case.topk_ids % 4 == 0)
+    tokens = np.random.default_rng(3).choice(512, 16, replace=False)
+    _layer_check(case, tokens=tokens)
+
+
+def test_pow2_activation_scales_glm():
+    shape = synth.LayerShape("glm_pow2", 256, 6144, 256, 8, act_fmt=synth.SCALE_FP32_POW2,
+                             routing="zipf", cfg_id=4)
+    case = synth.make_case("glm_pow2", 256, shape=shape)
+    tokens = np.random.default_rng(5).choice(256, 12, replace=False)
+    _layer_check(case, tokens=tokens)
+
+
+def test_deterministic():
+    case = synth.make_case("decode", 4)
+    o1, _, _ = run_forward(case)
+    o2, _, _ = run_forward(case)
+    torch.cuda.synchronize()
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
+def test_graph_replay_changing_routing():
+    """Capture once, then change routing and the live-token count in place between replays."""
+    shape = synth.small_shape("graph", E=16, H=512, I=256, topk=4)
+    case = synth.make_case("graph", 48, 48, shape=shape)
+    dev = device_case(case)
+    ws = moe.alloc_workspace(48, 16, 512, 256, 4)
+    out = torch.empty((48, 512), dtype=torch.bfloat16, device="cuda")
+    args = moe.make_args(dev["x"], dev["ids"], dev["w"], dev["w13"], dev["s13"], dev["w2"], dev["s2"],
+                         out, E=16, H=512, I=256, topk=4, M_cap=48, d_num_tokens=dev["n"])
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        moe.forward(args, ws, s)           # warm-up outside capture
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.forward(args, ws, s)
+    rng = np.random.default_rng(77)
+    for n in (48, 17, 1):
+        ids, w = synth.make_routing("softmax", 48, 16, 4, rng)
+        case.topk_ids[:] = ids
+        case.topk_weights[:] = w
+        case.n = n
+        dev["ids"].copy_(torch.from_numpy(ids))
+        dev["w"].copy_(torch.from_numpy(w))
+        dev["n"].fill_(n)
+        out.view(torch.int16).fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        gpu = bf16_tensor_to_f32(out)
+        ref = oracle_forward(case)
+        assert_layer_close(gpu[:n], ref, f"replay n={n}")
+        assert bool((out[n:].view(torch.int16) == -1).all())
