@@ -1,0 +1,464 @@
+"""Benchmark of the block-FP8 MoE layer forward on GB300.
+
+Workload (default): the decode-sized layer -- 288 experts, hidden 4096, intermediate 512, top-8,
+SwiGLU clamped at 7.0, FP8 E4M3 weights with 128x128 fp32 block scales, BF16 activations,
+softmax top-8 routing -- at M = 32 live tokens; the M = 1 and M = 4 points of the same workload
+are measured in the same run ("sweep").  One step = one full layer forward (routing alignment,
+activation quantization, FC1 + SwiGLU + requant, FC2, top-k reduce) replayed from a CUDA graph,
+with L2 flushed (a 512 MB write, larger than the 129 MB L2) before every step; the step time is
+taken with CUDA events around the replay on the launching stream.
+
+Prints one JSON line.  `--impl reference` times the CPU oracle on the host cores instead (the
+reference arm).  Under torchrun every rank runs its own replica of the layer on its own batch
+(weak scaling: the layer has no exchange step between data-parallel replicas); rank 0 prints the
+max over ranks.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+
+METRIC = "MoE layer us and % of FP8/HBM roofline vs live tokens M (1 GB300)"
+WORKLOAD = "decode"
+SWEEP_M = (1, 4, 32)
+KERNELS = ("align", "quant", "fc1", "fc2", "reduce")
+FLUSH_BYTES = 512 << 20
+
+
+# ------------------------------------------------------------------ peaks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def fp8_peak_tflops(peaks):
+    # dense FP8 = 2x dense BF16 on this part (nominal 4.5 vs 2.25 PFLOP/s)
+    return 2.0 * peaks["bf16_tflops"]
+
+
+# ------------------------------------------------------- algorithmic work
+def layer_work(case: synth.LayerCase):
+    """Algorithmic FLOPs and bytes of one layer forward and of its FC1 launch.
+
+    Layer bytes: weights (codes + block scales) of the occupied experts only, x in and out in
+    BF16, ids and routing weights; intermediates are not counted.  FC1 launch bytes: the occupied
+    experts' W13 codes + scales, the FP8 activation rows and scales it reads, and the FC2-input
+    codes and scales it writes.
+    """
+    sh = case.shape
+    ids = case.topk_ids[: case.n]
+    valid = ids[(ids >= 0) & (ids < sh.E)]
+    occ = int(np.unique(valid).size)
+    P = int(valid.size)
+    H, I = sh.H, sh.I
+    sc = 1 if sh.weight_fmt == synth.SCALE_UE8M0 else 4
+    asc = 1 if sh.act_fmt == synth.SCALE_UE8M0 else 4
+    w13_bytes = 2 * I * H + sc * (2 * I // 128) * (H // 128)
+    w2_bytes = H * I + sc * (H // 128) * (I // 128)
+    return {
+        "occupied_experts": occ, "pairs": P,
+        "flops": 6.0 * P * H * I,
+        "layer_bytes": occ * (w13_bytes + w2_bytes) + 4 * case.n * H + 8 * case.n * sh.topk,
+        "fc1_bytes": occ * w13_bytes + P * (H + asc * H // 128) + P * (I + asc * I // 128),
+        "fc1_flops": 4.0 * P * H * I,
+    }
+
+
+# ----------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi sampling of the SM clock and throttle reasons while the GPU works."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int, period_ms: int = 20):
+        self.lines = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", str(period_ms)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+                power.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm),
+                "power_w_max": max(power) if power else None}
+
+
+# ------------------------------------------------------------- ncu traffic
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_fp8_mixture_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(key: str):
+    """DRAM bytes per launch from the committed ncu summary, when it was taken on these sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f)
+    except (OSError, ValueError):
+        return None
+    entry = rec.get(key)
+    if not entry or entry.get("source_hash") != kernel_source_hash():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+# ------------------------------------------------------------ our arm
+class DecodeBench:
+    def __init__(self, M, rank, weights, dev_weights):
+        import torch
+        import block_fp8_mixture_gb300 as moe
+        self.moe = moe
+        self.M = M
+        self.case = synth.make_case(WORKLOAD, M, seed=2000 + M + 7919 * rank, weights=weights)
+        sh = self.case.shape
+        self.sh = sh
+        self.x = torch.from_numpy(self.case.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
+        self.ids = torch.from_numpy(self.case.topk_ids).cuda()
+        self.wts = torch.from_numpy(self.case.topk_weights).cuda()
+        self.w13, self.s13, self.w2, self.s2 = dev_weights
+        self.layer = moe.MoELayer(self.w13, self.s13, self.w2, self.s2, weight_fmt=sh.weight_fmt,
+                                  act_fmt=sh.act_fmt, clamp_mode=sh.clamp_mode,
+                                  clamp_limit=sh.limit, max_tokens=M, topk=sh.topk)
+        self.out = torch.empty((M, sh.H), dtype=torch.bfloat16, device="cuda")
+        self.args = self.layer.args(self.x, self.ids, self.wts, self.out)
+        self.ws = self.layer.workspace
+
+    def forward(self, stream):
+        self.moe.forward(self.args, self.ws, stream)
+
+    def steps(self, stream):
+        """The five steps as separate C-ABI calls (same kernels as forward())."""
+        moe, sh, ws = self.moe, self.sh, self.ws
+        return [
+            lambda: moe.align(self.ids, sh.E, sh.H, sh.I, ws, act_fmt=sh.act_fmt, stream=stream),
+            lambda: moe.quant_act(self.x, sh.topk, sh.E, sh.I, ws, act_fmt=sh.act_fmt, stream=stream),
+            lambda: moe.fc1_swiglu_quant(self.args, ws, stream),
+            lambda: moe.fc2(self.args, ws, stream),
+            lambda: moe.topk_reduce(self.args, ws, stream),
+        ]
+
+
+def run_ours(args, rank, world):
+    import torch
+    import block_fp8_mixture_gb300 as moe
+
+    moe.load_library()
+    torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", "0")))
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    peaks = load_peaks()
+    shape = synth.SHAPES[WORKLOAD]
+    weights = synth.make_weights(shape)
+    dev_w = tuple(torch.from_numpy(a).cuda() for a in (weights.w13, weights.s13, weights.w2, weights.s2))
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.Stream()
+    sweep = sorted(set(SWEEP_M) | {args.M}) if not (args.no_sweep or args.profile_run) else [args.M]
+    benches = {M: DecodeBench(M, rank, weights, dev_w) for M in sweep}
+
+    # graphs of the whole forward, one per M
+    graphs = {}
+    with torch.cuda.stream(stream):
+        for M, b in benches.items():
+            b.forward(stream)
+            stream.synchronize()
+            assert moe.last_device_status(b.ws, stream) == moe.MOE_OK
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                b.forward(stream)
+            graphs[M] = g
+    torch.cuda.synchronize()
+
+    def timed_graph(M, steps, warmup):
+        g = graphs[M]
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(warmup + steps):
+                flush.fill_(i & 0xFF)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                g.replay()
+                e1.record(stream)
+                if i >= warmup:
+                    times.append((e0, e1))
+        stream.synchronize()
+        return [a.elapsed_time(b) * 1e3 for a, b in times]   # us
+
+    def per_kernel(M, steps):
+        b = benches[M]
+        fns = b.steps(stream)
+        acc = {k: [] for k in KERNELS}
+        with torch.cuda.stream(stream):
+            for i in range(steps + 2):
+                flush.fill_(i & 0xFF)
+                if hasattr(torch.cuda, "_sleep"):
+                    torch.cuda._sleep(2_000_000)   # let the host queue the launches ahead
+                evs = [torch.cuda.Event(enable_timing=True) for _ in range(len(fns) + 1)]
+                evs[0].record(stream)
+                for f, e in zip(fns, evs[1:]):
+                    f()
+                    e.record(stream)
+                stream.synchronize()
+                if i >= 2:
+                    for k, a, c in zip(KERNELS, evs[:-1], evs[1:]):
+                        acc[k].append(a.elapsed_time(c) * 1e3)
+        return {k: statistics.mean(v) for k, v in acc.items()}
+
+    def e2e(M, steps, warmup):
+        b = benches[M]
+        x_h = b.x.cpu().pin_memory()
+        ids_h = b.ids.cpu().pin_memory()
+        w_h = b.wts.cpu().pin_memory()
+        out_h = torch.empty(b.out.shape, dtype=b.out.dtype).pin_memory()
+        x_d, ids_d, w_d = torch.empty_like(b.x), torch.empty_like(b.ids), torch.empty_like(b.wts)
+        out_d = torch.empty_like(b.out)
+        times = []
+        with torch.cuda.stream(stream):
+            for i in range(warmup + steps):
+                flush.fill_(i & 0xFF)
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                x_d.copy_(x_h, non_blocking=True)
+                ids_d.copy_(ids_h, non_blocking=True)
+                w_d.copy_(w_h, non_blocking=True)
+                b.layer(x_d, ids_d, w_d, out=out_d, stream=stream)
+                out_h.copy_(out_d, non_blocking=True)
+                e1.record(stream)
+                stream.synchronize()
+                if i >= warmup:
+                    times.append(e0.elapsed_time(e1) * 1e3)
+        h2d = x_h.numel() * 2 + ids_h.numel() * 4 + w_h.numel() * 4
+        d2h = out_h.numel() * 2
+        return statistics.mean(times), h2d, d2h
+
+    if args.profile_run:
+        us = timed_graph(args.M, args.steps, args.warmup)
+        return {"profile_run": True, "M": args.M, "us_mean": statistics.mean(us)}
+
+    # pre-warm (clocks settle), then the timed region of the headline M
+    clock = ClockSampler(torch.cuda.current_device())
+    t_end = time.time() + 0.5
+    while time.time() < t_end:
+        timed_graph(args.M, 20, 0)
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    us = timed_graph(args.M, args.steps, args.warmup)
+    torch.cuda.synchronize()
+    if dist is not None:
+        dist.barrier()
+    wall = time.perf_counter() - t0
+    clocks = clock.stop()
+
+    us_mean = statistics.mean(us)
+    if dist is not None:
+        t = torch.tensor([us_mean], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        us_mean = float(t.item())
+
+    work = layer_work(benches[args.M].case)
+    kern = per_kernel(args.M, max(10, min(args.steps, 50)))
+    fc1_us = kern["fc1"]
+    hbm_peak = peaks["hbm_gbs"]
+    fc1_gbs = work["fc1_bytes"] / (fc1_us * 1e-6) / 1e9
+    traffic = ncu_traffic(f"fc1_decode_M{args.M}")
+    roofline = {"kernel": "fc1 (grouped GEMM + SwiGLU + requant)", "bound": "hbm",
+                "achieved": fc1_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": fc1_gbs / hbm_peak,
+                "traffic": traffic, "algorithmic_bytes": work["fc1_bytes"],
+                "avg_launch_us": fc1_us, "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)"}
+
+    def layer_roof(M, t_us):
+        w = layer_work(benches[M].case)
+        t_f = w["flops"] / (fp8_peak_tflops(peaks) * 1e12)
+        t_b = w["layer_bytes"] / (hbm_peak * 1e9)
+        return {"us": t_us, "roofline_us": max(t_f, t_b) * 1e6,
+                "frac_of_roofline": max(t_f, t_b) * 1e6 / t_us,
+                "bound": "tensor" if t_f > t_b else "hbm",
+                "tflops": w["flops"] / (t_us * 1e-6) / 1e12,
+                "gbs": w["layer_bytes"] / (t_us * 1e-6) / 1e9,
+                "occupied_experts": w["occupied_experts"]}
+
+    sweep_out = {}
+    for M in sweep:
+        t_us = us_mean if M == args.M else statistics.mean(timed_graph(M, max(20, args.steps // 2), 3))
+        sweep_out[str(M)] = layer_roof(M, t_us)
+    sweep_out[str(args.M)]["per_kernel_us"] = kern
+
+    e2e_us, h2d, d2h = e2e(args.M, max(10, min(args.steps, 100)), 3)
+
+    line = {
+        "metric": METRIC, "value": us_mean, "unit": "us", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": us_mean / 1e3, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
+        "config": {"workload": f"decode MoE layer E=288 H=4096 I=512 top-8 M={args.M}",
+                   "clamp": "SwiGLU clamp 7.0 before SiLU", "scales": "fp32 128x128 weight, fp32 1x128 act",
+                   "l2": "flushed before every step (512 MB write)", "timing": "CUDA graph replay, CUDA events",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": roofline,
+        "layer_roofline": sweep_out[str(args.M)],
+        "sweep": sweep_out,
+        "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "api": "MoELayer.__call__ (C ABI moe_fp8_block_forward), pinned host buffers"},
+        "gpu_launches": len(KERNELS) * args.steps,
+        "clocks": clocks,
+        "timed_wall_s": wall,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(benches[args.M].case)
+    if dist is not None:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------- the oracle arm
+def cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def oracle_tokens(case: synth.LayerCase, tokens):
+    import oracle
+    sh, w = case.shape, case.weights
+    return oracle.moe_forward(case.x, case.topk_ids, case.topk_weights, w.w13, w.s13, w.w2, w.s2,
+                              act_fmt=sh.act_fmt, weight_fmt=sh.weight_fmt,
+                              clamp_mode=sh.clamp_mode, limit=sh.limit, tokens=tokens)
+
+
+def time_oracle(case: synth.LayerCase, budget_s: float, max_tokens=None):
+    """Seconds per token of the oracle (as it stands), timed token by token on a sample of the
+    case's tokens until about budget_s has been spent."""
+    order = np.random.default_rng(0).permutation(case.n)
+    limit = case.n if max_tokens is None else min(case.n, max_tokens)
+    done, spent = 0, 0.0
+    while done < limit and (spent < budget_s or done == 0):
+        t0 = time.perf_counter()
+        oracle_tokens(case, order[done: done + 1])
+        spent += time.perf_counter() - t0
+        done += 1
+    return spent / done, done
+
+
+def cpu_baseline(case: synth.LayerCase, budget_s: float = 12.0):
+    sec_tok, done = time_oracle(case, budget_s)
+    us_layer = sec_tok * case.n * 1e6
+    return {"value": us_layer, "unit": "us", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"{done} of the {case.n} tokens of the same layer, one at a time, "
+                      f"time per token x {case.n} (numpy, BLAS default threads)"}
+
+
+def reference_arm(args):
+    weights = synth.make_weights(synth.SHAPES[WORKLOAD])
+    case = synth.make_case(WORKLOAD, args.M, seed=2000 + args.M, weights=weights)
+    per_step = []
+    for _ in range(args.warmup + args.steps):
+        sec_tok, _ = time_oracle(case, 0.0, max_tokens=1)
+        per_step.append(sec_tok)
+    us_layer = statistics.mean(per_step[args.warmup:]) * case.n * 1e6
+    return {
+        "impl": "reference", "metric": METRIC, "value": us_layer, "unit": "us",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": us_layer / 1e3, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
+        "config": {"workload": f"decode MoE layer E=288 H=4096 I=512 top-8 M={args.M}"},
+        "cpu_baseline": {"value": us_layer, "unit": "us", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": f"per step: 1 token of the M={args.M} layer, time x {case.n}"},
+        "e2e": {"value": us_layer, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--M", type=int, default=32, help="live tokens of the headline point")
+    ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-run", action="store_true",
+                    help="only W + K graph replays of the headline point (for ncu captures)")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(reference_arm(args)), flush=True)
+        return 0
+    line = run_ours(args, rank, world)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
