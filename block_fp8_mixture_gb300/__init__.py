@@ -40,9 +40,10 @@ class MoeError(RuntimeError):
 class WsPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "num_tiles", "seg_start", "live_end", "sorted_pair", "pair_row", "tile_expert",
-        "a1_q", "a1_s", "a2_q", "a2_s", "y", "splitk_partial", "splitk_count", "total_bytes")] + [
-        ("R_cap", ctypes.c_int32), ("T_cap", ctypes.c_int32), ("P_cap", ctypes.c_int32),
-        ("fc1_ksplit", ctypes.c_int32)]
+        "num_chunks", "chunk_row0", "a1_q", "a1_s", "a2_q", "a2_s", "y", "splitk_partial",
+        "splitk_count", "total_bytes")] + [
+        ("R_cap", ctypes.c_int32), ("T_cap", ctypes.c_int32), ("C_cap", ctypes.c_int32),
+        ("P_cap", ctypes.c_int32), ("fc1_ksplit", ctypes.c_int32), ("small_batch", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}
@@ -155,6 +156,8 @@ def workspace_views(ws, M_cap: int, E: int, H: int, I: int, topk: int, act_fmt: 
         "sorted_pair": view(p["sorted_pair"], R, torch.int32, 4),
         "pair_row": view(p["pair_row"], P, torch.int32, 4),
         "tile_expert": view(p["tile_expert"], T, torch.int32, 4),
+        "num_chunks": view(p["num_chunks"], 1, torch.int32, 4),
+        "chunk_row0": view(p["chunk_row0"], p["C_cap"], torch.int32, 4),
         "a1_q": view(p["a1_q"], R * H, torch.uint8, 1).view(R, H),
         "a1_s": view(p["a1_s"], (H // 128) * R, sdt, ssz).view(H // 128, R),
         "a2_q": view(p["a2_q"], R * I, torch.uint8, 1).view(R, I),

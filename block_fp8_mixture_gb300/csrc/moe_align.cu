@@ -21,6 +21,34 @@ namespace moe {
 
 constexpr int kAlignThreads = 1024;
 constexpr int kAlignWarps = kAlignThreads / 32;
+constexpr int kChunkRows = 32;
+
+// Exclusive scan of one int per thread over the 1024-thread CTA; *total gets the sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int t = __shfl_up_sync(0xFFFFFFFFu, incl, d);
+    if (lane >= d) incl += t;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = warp_sums[lane];
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+      const int t = __shfl_up_sync(0xFFFFFFFFu, w, d);
+      if (lane >= d) w += t;
+    }
+    warp_sums[lane] = w;
+  }
+  __syncthreads();
+  const int excl = incl - v + (warp > 0 ? warp_sums[warp - 1] : 0);
+  *total = warp_sums[kAlignWarps - 1];
+  __syncthreads();
+  return excl;
+}
 
 __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
   extern __shared__ int32_t sm[];
@@ -34,6 +62,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
   const int lane = tid & 31;
   const uint32_t lanes_below = (1u << lane) - 1u;
 
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   int n = p.M_cap;
   if (p.d_num_tokens != nullptr) n = min(max(*p.d_num_tokens, 0), p.M_cap);
   const int num_pairs = n * p.topk;
@@ -75,40 +105,24 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
     padded = (run + kAlign - 1) / kAlign * kAlign;
   }
   // exclusive scan of padded counts (E <= 1024 = one expert per thread)
-  int incl = padded;
-#pragma unroll
-  for (int d = 1; d < 32; d <<= 1) {
-    const int v = __shfl_up_sync(0xFFFFFFFFu, incl, d);
-    if (lane >= d) incl += v;
-  }
-  if (lane == 31) warp_sums[warp] = incl;
-  __syncthreads();
-  if (warp == 0) {
-    int w = warp_sums[lane];
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-      const int v = __shfl_up_sync(0xFFFFFFFFu, w, d);
-      if (lane >= d) w += v;
-    }
-    warp_sums[lane] = w;                           // inclusive over warps
-  }
-  __syncthreads();
-  const int excl = incl - padded + (warp > 0 ? warp_sums[warp - 1] : 0);
-  int count = 0;
-  if (tid < E) {
-    count = seg[tid];
-  }
-  __syncthreads();
+  int total = 0;
+  const int excl = block_exclusive_scan(padded, warp_sums, &total);
+  const int count = tid < E ? seg[tid] : 0;
+  // live 32-row chunks of each expert (the small-batch schedule's work list)
+  int chunk_total = 0;
+  const int chunk_base = block_exclusive_scan((count + kChunkRows - 1) / kChunkRows, warp_sums,
+                                              &chunk_total);
   if (tid < E) {
     seg[tid] = excl;
     p.seg_start[tid] = excl;
     p.live_end[tid] = excl + count;
+    for (int c = 0; c * kChunkRows < count; ++c) p.chunk_row0[chunk_base + c] = excl + c * kChunkRows;
   }
   if (tid == 0) {
-    const int total = warp_sums[kAlignWarps - 1];
     seg[E] = total;
     p.seg_start[E] = total;
     *p.num_tiles = total / kAlign;
+    *p.num_chunks = chunk_total;
   }
   __syncthreads();
 
@@ -147,8 +161,7 @@ cudaError_t launch_align(const AlignParams& p, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
-  k_align<<<1, kAlignThreads, smem, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_align, dim3(1), dim3(kAlignThreads), smem, s, p);
 }
 
 }  // namespace moe

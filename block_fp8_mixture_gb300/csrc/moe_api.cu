@@ -12,14 +12,22 @@ namespace moe {
 
 static inline size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// FC1 K-split for small batches: enough CTAs to stream the occupied experts' weights from HBM.
-// Upper bound of live tiles = min(E, P_cap); target about two CTAs per SM of a 152-SM part.
-static int choose_fc1_ksplit(int E, int H, int I, int P_cap) {
-  if (P_cap > 1024) return 1;
-  const long items = (long)std::min(E, P_cap) * (I / kGroup);
+// Small-batch schedule (tokens on the MMA's N side, 32-row chunks) when the average expert holds at
+// most 16 rows; otherwise 128-row tiles.
+static bool use_small_batch(int E, long long P_cap) { return P_cap > 0 && P_cap <= 16LL * E; }
+
+// FC1 K-split of the small-batch schedule.  Splitting K costs a fix-up round trip per item, so it
+// only pays when the occupied experts give too few work items to keep the SMs streaming: split until
+// the estimated items (at most min(E, P_cap) experts x I/128 column blocks) reach half of a 152-SM
+// part, keeping at least two K blocks per split and the fp32 partials under 256 MB.
+static int choose_fc1_ksplit(int E, int H, int I, long long P_cap, bool small) {
+  if (!small) return 1;
+  const long long items = std::min<long long>(E, P_cap) * (I / kGroup);
   const int kb = H / kGroup;
   int ks = 1;
-  while (ks < 8 && items * ks * 2 <= 304 && kb % (ks * 2) == 0) ks *= 2;
+  while (ks < kMaxKSplit && items * ks < 76 && kb % (ks * 2) == 0 && kb / (ks * 2) >= 2 &&
+         (long long)(ks * 2) * P_cap * 2 * I * 4 <= (256LL << 20))
+    ks *= 2;
   return ks;
 }
 
@@ -43,7 +51,9 @@ moe_status make_plan(int M_cap, int E, int H, int I, int topk, int act_fmt, Plan
   w.P_cap = (int32_t)P_cap;
   w.R_cap = (int32_t)R_cap;
   w.T_cap = (int32_t)(R_cap / kAlign);
-  w.fc1_ksplit = choose_fc1_ksplit(E, H, I, (int)P_cap);
+  w.C_cap = (int32_t)(R_cap / 32);
+  w.small_batch = use_small_batch(E, P_cap) ? 1 : 0;
+  w.fc1_ksplit = choose_fc1_ksplit(E, H, I, P_cap, w.small_batch != 0);
   const size_t sc = act_fmt == MOE_SCALE_UE8M0 ? 1 : 4;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -58,13 +68,15 @@ moe_status make_plan(int M_cap, int E, int H, int I, int topk, int act_fmt, Plan
   w.sorted_pair = take((size_t)R_cap * 4);
   w.pair_row = take((size_t)P_cap * 4);
   w.tile_expert = take((size_t)w.T_cap * 4);
+  w.num_chunks = take(4);
+  w.chunk_row0 = take((size_t)w.C_cap * 4);
   w.a1_q = take((size_t)R_cap * H);
   w.a1_s = take((size_t)(H / kGroup) * R_cap * sc);
   w.a2_q = take((size_t)R_cap * I);
   w.a2_s = take((size_t)(I / kGroup) * R_cap * sc);
   w.y = take((size_t)R_cap * H * 2);
   w.splitk_partial = take(w.fc1_ksplit > 1 ? (size_t)w.fc1_ksplit * P_cap * 2 * I * 4 : 0);
-  w.splitk_count = take(w.fc1_ksplit > 1 ? (size_t)w.T_cap * (I / kGroup) * 4 : 0);
+  w.splitk_count = take(w.fc1_ksplit > 1 ? (size_t)w.C_cap * (I / kGroup) * 4 : 0);
   w.total_bytes = off;
   plan->M_cap = M_cap;
   plan->E = E;
@@ -110,6 +122,21 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Flat array of n elements (fp32 or bytes), boxes of 16 bytes: used to fetch one block scale (and
+// its 16-byte aligned neighbours) per pipeline stage.
+static bool make_map_1d(CUtensorMap* m, const void* base, bool bytes, uint64_t n) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[1] = {n};
+  const cuuint64_t strides[1] = {0};
+  const cuuint32_t box[1] = {bytes ? 16u : 4u};
+  const cuuint32_t estr[1] = {1};
+  return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static int sm_count() {
   int dev = 0, n = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 148;
@@ -140,7 +167,6 @@ static moe_status check_args(const moe_fwd_args* a, const void* ws, size_t ws_by
   if (st != MOE_OK) return st;
   st = check_ws(*pl, ws, ws_bytes);
   if (st != MOE_OK) return st;
-  const size_t wsc = a->weight_scale_fmt == MOE_SCALE_UE8M0 ? 1 : 4;
   if (a->d_num_tokens != nullptr && !aligned(a->d_num_tokens, 4)) return MOE_ERR_INVALID_ARG;
   if (need_x) {
     if (a->x == nullptr || !aligned(a->x, 16)) return MOE_ERR_INVALID_ARG;
@@ -148,11 +174,11 @@ static moe_status check_args(const moe_fwd_args* a, const void* ws, size_t ws_by
   }
   if (need_w13) {
     if (a->w13 == nullptr || !aligned(a->w13, 16)) return MOE_ERR_INVALID_ARG;
-    if (a->s13 == nullptr || !aligned(a->s13, wsc)) return MOE_ERR_INVALID_ARG;
+    if (a->s13 == nullptr || !aligned(a->s13, 16)) return MOE_ERR_INVALID_ARG;
   }
   if (need_w2) {
     if (a->w2 == nullptr || !aligned(a->w2, 16)) return MOE_ERR_INVALID_ARG;
-    if (a->s2 == nullptr || !aligned(a->s2, wsc)) return MOE_ERR_INVALID_ARG;
+    if (a->s2 == nullptr || !aligned(a->s2, 16)) return MOE_ERR_INVALID_ARG;
   }
   if (need_reduce) {
     if (a->topk_weights == nullptr || !aligned(a->topk_weights, 4)) return MOE_ERR_INVALID_ARG;
@@ -183,7 +209,9 @@ static moe_status run_align(const int32_t* ids, const int32_t* d_n, const Plan& 
   p.num_tiles = at<int32_t>(ws, pl.ws.num_tiles);
   p.status = at<int32_t>(ws, pl.ws.status);
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
-  p.splitk_count_len = pl.ws.fc1_ksplit > 1 ? pl.ws.T_cap * (pl.I / kGroup) : 0;
+  p.splitk_count_len = pl.ws.fc1_ksplit > 1 ? pl.ws.C_cap * (pl.I / kGroup) : 0;
+  p.chunk_row0 = at<int32_t>(ws, pl.ws.chunk_row0);
+  p.num_chunks = at<int32_t>(ws, pl.ws.num_chunks);
   return launch_align(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -215,13 +243,17 @@ static void fill_gemm_common(GemmParams& p, const Plan& pl, void* ws) {
   p.a_scale_ue8m0 = pl.act_fmt == MOE_SCALE_UE8M0;
   p.P_cap = pl.ws.P_cap;
   p.sorted_pair = at<int32_t>(ws, pl.ws.sorted_pair);
+  p.chunk_row0 = at<int32_t>(ws, pl.ws.chunk_row0);
+  p.num_chunks = at<int32_t>(ws, pl.ws.num_chunks);
 }
 
 static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {
   if (pl.ws.R_cap == 0) return MOE_OK;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmS;
+  const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
   if (!make_map_u8(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kABoxRows) ||
-      !make_map_u8(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup))
+      !make_map_u8(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup) ||
+      !make_map_1d(&tmS, a->s13, w_ue, (uint64_t)pl.E * (2 * pl.I / kGroup) * (pl.H / kGroup)))
     return MOE_ERR_CUDA;
   GemmParams p;
   fill_gemm_common(p, pl, ws);
@@ -239,16 +271,21 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.clamp_limit = a->clamp_limit;
   p.splitk_partial = at<float>(ws, pl.ws.splitk_partial);
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
-  const long items = (long)pl.ws.T_cap * p.n_blocks * p.ksplit;
+  const bool small = pl.ws.small_batch != 0;
+  const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks * p.ksplit;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
-  return launch_fc1(tmA, tmB, p, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const cudaError_t err = small ? launch_fc1_small(tmA, tmB, tmS, p, grid, s)
+                                : launch_fc1(tmA, tmB, tmS, p, grid, s);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {
   if (pl.ws.R_cap == 0) return MOE_OK;
-  CUtensorMap tmA, tmB;
+  CUtensorMap tmA, tmB, tmS;
+  const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
   if (!make_map_u8(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kABoxRows) ||
-      !make_map_u8(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup))
+      !make_map_u8(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup) ||
+      !make_map_1d(&tmS, a->s2, w_ue, (uint64_t)pl.E * (pl.H / kGroup) * (pl.I / kGroup)))
     return MOE_ERR_CUDA;
   GemmParams p;
   fill_gemm_common(p, pl, ws);
@@ -261,9 +298,12 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.out_cols = pl.H;
   p.ksplit = 1;
   p.y = at<uint16_t>(ws, pl.ws.y);
-  const long items = (long)pl.ws.T_cap * p.n_blocks;
+  const bool small = pl.ws.small_batch != 0;
+  const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
-  return launch_fc2(tmA, tmB, p, grid, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
+                                : launch_fc2(tmA, tmB, tmS, p, grid, s);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 static moe_status run_reduce(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {

@@ -32,6 +32,19 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t nthread
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ------------------------------------------------- programmatic dependent launch
+// Wait until the preceding kernels of the stream have completed and their writes are visible.  Every
+// kernel calls this before it reads or writes global memory another kernel of the layer touches.
+__device__ __forceinline__ void grid_dep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Let the next kernel of the stream begin launching (it still waits in grid_dep_wait for this
+// kernel to complete before touching shared data).
+__device__ __forceinline__ void grid_dep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- mbarrier
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
@@ -101,6 +114,26 @@ __device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
       " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+// 1-D tiled bulk tensor load (a box of a flat array; elements past the end read as zero).
+__device__ __forceinline__ void tma_load_1d(uint32_t dst, const CUtensorMap* map, int x,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.1d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2}], [%3];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(bar)
+      : "memory");
+}
+
+// Plain bulk copy global -> shared (16-byte aligned addresses, size a multiple of 16).
+__device__ __forceinline__ void bulk_copy_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                              uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
       : "memory");
 }
 
@@ -242,6 +275,12 @@ __device__ __forceinline__ float load_scale(const void* base, size_t idx, int is
     return __uint_as_float(b << 23);
   }
   return static_cast<const float*>(base)[idx];
+}
+
+// Scale value held in shared memory (fp32 word or UE8M0 byte) at element idx.
+__device__ __forceinline__ float smem_scale_at(const uint8_t* base, int idx, int is_ue8m0) {
+  if (is_ue8m0) return __uint_as_float((uint32_t)base[idx] << 23);
+  return reinterpret_cast<const float*>(base)[idx];
 }
 
 __device__ __forceinline__ void store_scale(void* base, size_t idx, float s, int is_ue8m0) {

@@ -10,17 +10,22 @@
 //
 // Work item = (live row tile, output column block, K split).  One CTA per SM walks items
 // blockIdx.x, blockIdx.x + gridDim.x, ...; inside the CTA:
-//   warp 0 (one lane)  TMA producer: per 128-wide K block, the tile's live activation rows (32-row
-//                      boxes, only those below the expert's live end) and 256 weight rows, into a
-//                      4-stage ring of 48 KB stages (128-byte swizzle).
+//   warp 0 (one lane)  TMA producer.  Per 128-wide K block one stage of a 4-stage ring receives
+//                      the tile's live activation rows (8-row boxes, only those below the
+//                      expert's live end), 256 weight rows (128-byte swizzle), the 128 activation
+//                      scales of the K block (bulk copy) and the two weight block scales (16-byte
+//                      boxes of a 1-D tensor map), all counted on the stage's mbarrier.
 //   warp 1 (one lane)  MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) per K block
 //                      into one of two 256-column fp32 accumulators in tensor memory.
-//   warps 2..9         promotion + epilogue: thread = one workspace row and 128 of the 256 columns;
-//                      per K block it loads its partial sums from tensor memory and accumulates
+//   warps 2..9         promotion + epilogue.  A thread owns one row and 128 of the 256 columns;
+//                      per K block it reads its partial sums from tensor memory and accumulates
 //                      acc = fma(partial, a_scale*b_scale, acc) in registers, then releases the
-//                      accumulator buffer so the MMA of the next K block overlaps the promotion.
+//                      accumulator so the MMA of a later K block overlaps the promotion.
+// Row placement: activation rows are loaded in 8-row groups; group j goes to tensor-memory lanes
+// 32*(j%4) + 8*(j/4) .. +7, so even a tile with 8..32 live rows keeps all four lane quarters (all
+// eight promotion warps) busy.
 // FC1 columns: 128 gate rows of W13 and the matching 128 up rows, so a thread owns 64 (gate, up)
-// pairs of one row and the SwiGLU and 1x128 requantization need only the row amax of the two
+// pairs of one row; the SwiGLU and the 1x128 requantization need only the row amax of the two
 // threads sharing the row.  FC2 columns: 256 consecutive hidden columns, BF16 out.
 // Small batches split K across CTAs (FC1 only): each split writes its fp32 partial rows, the last
 // split to arrive (atomic counter per item) sums the splits in fixed order and runs the epilogue.
@@ -47,13 +52,30 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
   return it;
 }
 
+// Weight block-scale rows of an item (indices into the [E][row blocks][K/128] scale array).
+// FC1: the gate block nb and the up block I/128 + nb.  FC2: hidden blocks 2nb and 2nb + 1.
+template <bool kFC1>
+__device__ __forceinline__ void scale_rows(const GemmParams& p, const Item& w, int& r0, int& r1,
+                                           bool& has_r1) {
+  const int ncb = p.b_rows_per_expert / kGroup;
+  if (kFC1) {
+    r0 = w.e * ncb + w.nb;
+    r1 = w.e * ncb + p.out_cols / kGroup + w.nb;
+    has_r1 = true;
+  } else {
+    r0 = w.e * ncb + 2 * w.nb;
+    r1 = r0 + 1;
+    has_r1 = 2 * w.nb + 1 < ncb;
+  }
+}
+
 // SiLU(g) * u with the optional clamp, fp32, IEEE division, no fused multiply-add.
 __device__ __forceinline__ float swiglu(float g, float u, int mode, float lim) {
   if (mode == MOE_CLAMP_BEFORE_SILU) {
     g = fminf(g, lim);
     u = fminf(fmaxf(u, -lim), lim);
   }
-  const float sig = __fdiv_rn(1.0f, __fadd_rn(1.0f, expf(-g)));
+  const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-g)));   // correctly rounded 1/(1+e^-g)
   float silu = __fmul_rn(g, sig);
   if (mode == MOE_CLAMP_AFTER_SILU) {
     silu = fminf(silu, lim);
@@ -84,12 +106,14 @@ __device__ __forceinline__ void promote32(uint32_t taddr, float sab, float* acc)
 template <bool kFC1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmS, const GemmParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_base);
-  uint8_t* ctrl = smem + kStages * kStageBytes;
+  uint8_t* slots = smem + kStages * kStageBytes;               // scale slots, 1024-aligned
+  uint8_t* ctrl = slots + kStages * kScaleSlotBytes;
+  const uint32_t slot0 = smem_addr(slots);
   const uint32_t bar0 = smem_addr(ctrl);
   // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
@@ -105,15 +129,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr int kEpiWarps = kEpiThreads / 32;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1);
+      // a stage is free once the MMAs read it and every promotion warp read its scales
+      mbar_init(empty_bar(s), 1 + kEpiWarps);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
-      mbar_init(tempty_bar(b), kEpiThreads / 32);
+      mbar_init(tempty_bar(b), kEpiWarps);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -124,17 +150,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmS);
   }
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
   tc_fence_before_sync();
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();                 // the previous kernel's outputs are complete from here on
+  grid_dep_launch_dependents();
 
   const int num_tiles = *p.num_tiles;
   const int total = num_tiles * p.n_blocks * p.ksplit;
-  const int kb_per_split = (p.K / kBK) / p.ksplit;
   const int KB = p.K / kBK;
+  const int kb_per_split = KB / p.ksplit;
+  const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
+  const int a_scale_bytes = a_ue ? kBM : kBM * 4;
+  const int w_per16 = b_ue ? 16 : 4;      // scale elements per 16-byte box
   int* status = p.status;
 
   int prod_issued = 0;
@@ -157,7 +189,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         brow1 = brow0 + kGroup;
         second = (w.nb * kBN + kGroup) < p.out_cols;
       }
-      const uint32_t bytes = nbox * (kABoxRows * kBK) + (second ? 2 : 1) * (kGroup * kBK);
+      int sr0, sr1;
+      bool has_sr1;
+      scale_rows<kFC1>(p, w, sr0, sr1, has_sr1);
+      const uint32_t bytes = nbox * (kABoxRows * kBK) + (second ? 2 : 1) * (kGroup * kBK) +
+                             a_scale_bytes + (has_sr1 ? 32 : 16);
       const int kb0 = w.ks * kb_per_split;
       for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
         const int s = it % kStages;
@@ -169,10 +205,21 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         mbar_arrive_expect_tx(full_bar(s), bytes);
         const uint32_t sA = sbase + s * kStageBytes;
         const uint32_t sB = sA + kABytes;
-        for (int q = 0; q < nbox; ++q)
-          tma_load_2d(sA + q * (kABoxRows * kBK), &tmA, kb * kBK, w.m0 + q * kABoxRows, full_bar(s));
+        const uint32_t sS = slot0 + s * kScaleSlotBytes;
+        for (int j = 0; j < nbox; ++j)
+          tma_load_2d(sA + (32 * (j & 3) + 8 * (j >> 2)) * kBK, &tmA, kb * kBK,
+                      w.m0 + j * kABoxRows, full_bar(s));
         tma_load_2d_hint(sB, &tmB, kb * kBK, brow0, full_bar(s), pol_w);
         if (second) tma_load_2d_hint(sB + kGroup * kBK, &tmB, kb * kBK, brow1, full_bar(s), pol_w);
+        bulk_copy_g2s(sS, static_cast<const uint8_t*>(p.a_scale) +
+                              ((size_t)kb * p.R_cap + w.m0) * (a_ue ? 1 : 4),
+                      a_scale_bytes, full_bar(s));
+        const int i0 = sr0 * KB + kb;
+        tma_load_1d(sS + kSlotWScale0, &tmS, i0 - i0 % w_per16, full_bar(s));
+        if (has_sr1) {
+          const int i1 = sr1 * KB + kb;
+          tma_load_1d(sS + kSlotWScale1, &tmS, i1 - i1 % w_per16, full_bar(s));
+        }
         ++it;
       }
     }
@@ -213,54 +260,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   } else if (warp >= kEpiWarp0) {
     // ---------------------------------------------------- promotion + epilogue
     const int ew = warp - kEpiWarp0;
-    const int wg = ew >> 2;          // which half of the 256 columns
-    const int q = warp & 3;          // TMEM lane quarter this warp may access
-    const int row = q * 32 + lane;   // row inside the tile
-    const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
-    const int ncb = p.b_rows_per_expert / kGroup;   // weight row blocks per expert
+    const int wg = ew >> 2;                        // which half of the 256 columns
+    const int q = warp & 3;                        // TMEM lane quarter this warp may access
+    const int row = 32 * (lane >> 3) + 8 * q + (lane & 7);   // tile row held in lane 32q + lane
     int c = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Item w = decode_item(p, item);
-      const bool qlive = q * 32 < w.live;
+      const bool qlive = 8 * q < w.live;
       const bool rlive = row < w.live;
+      int sr0, sr1;
+      bool has_sr1;
+      scale_rows<kFC1>(p, w, sr0, sr1, has_sr1);
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
       const int kb0 = w.ks * kb_per_split;
       for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
         const int b = c & 1;
-        const uint32_t ph = (c >> 1) & 1;
-        float sa = 0.0f, sw0 = 0.0f, sw1 = 0.0f;
-        if (qlive) {
-          sa = load_scale(p.a_scale, (size_t)kb * p.R_cap + w.m0 + row, a_ue);
-          if (kFC1) {
-            sw0 = load_scale(p.b_scale, ((size_t)w.e * ncb + w.nb) * KB + kb, b_ue);
-            sw1 = load_scale(p.b_scale, ((size_t)w.e * ncb + p.out_cols / kGroup + w.nb) * KB + kb, b_ue);
-          } else {
-            const int hb = w.nb * 2 + wg;
-            sw0 = hb < ncb ? load_scale(p.b_scale, ((size_t)w.e * ncb + hb) * KB + kb, b_ue) : 0.0f;
-          }
-        }
-        if (!mbar_wait(tfull_bar(b), ph, abort_flag, status)) {
+        const int s = c % kStages;
+        if (!mbar_wait(tfull_bar(b), (c >> 1) & 1, abort_flag, status) ||
+            !mbar_wait(full_bar(s), (c / kStages) & 1, abort_flag, status)) {
           ok = false;
           break;
         }
+        float sab0 = 0.0f, sab1 = 0.0f;
+        if (qlive) {
+          const uint8_t* slot = slots + s * kScaleSlotBytes;
+          const float sa = smem_scale_at(slot, row, a_ue);
+          const int i0 = sr0 * KB + kb, i1 = sr1 * KB + kb;
+          const float sw0 = smem_scale_at(slot + kSlotWScale0, i0 % w_per16, b_ue);
+          const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotWScale1, i1 % w_per16, b_ue) : 0.0f;
+          sab0 = __fmul_rn(sa, sw0);
+          sab1 = __fmul_rn(sa, sw1);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_bar(s));
         tc_fence_after_sync();
         if (qlive) {
           const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
           if (kFC1) {
-            const float sg = __fmul_rn(sa, sw0), su = __fmul_rn(sa, sw1);
-            promote32(t0 + wg * 64, sg, acc);
-            promote32(t0 + wg * 64 + 32, sg, acc + 32);
-            promote32(t0 + kGroup + wg * 64, su, acc + 64);
-            promote32(t0 + kGroup + wg * 64 + 32, su, acc + 96);
+            promote32(t0 + wg * 64, sab0, acc);
+            promote32(t0 + wg * 64 + 32, sab0, acc + 32);
+            promote32(t0 + kGroup + wg * 64, sab1, acc + 64);
+            promote32(t0 + kGroup + wg * 64 + 32, sab1, acc + 96);
           } else {
-            const float s = __fmul_rn(sa, sw0);
-            promote32(t0 + wg * 128, s, acc);
-            promote32(t0 + wg * 128 + 32, s, acc + 32);
-            promote32(t0 + wg * 128 + 64, s, acc + 64);
-            promote32(t0 + wg * 128 + 96, s, acc + 96);
+            const float sab = wg == 0 ? sab0 : sab1;
+            promote32(t0 + wg * 128, sab, acc);
+            promote32(t0 + wg * 128 + 32, sab, acc + 32);
+            promote32(t0 + wg * 128 + 64, sab, acc + 64);
+            promote32(t0 + wg * 128 + 96, sab, acc + 96);
           }
         }
         tc_fence_before_sync();
@@ -390,23 +439,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 }
 
 template <bool kFC1>
-static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                               int grid, cudaStream_t s) {
+static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                               const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<kFC1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
   if (err != cudaSuccess) return err;
-  k_grouped_gemm<kFC1><<<grid, kGemmThreads, kGemmSmemBytes, s>>>(tmA, tmB, p);
-  return cudaGetLastError();
+  return launch_pdl(k_grouped_gemm<kFC1>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, s, tmA, tmB,
+                    tmS, p);
 }
 
-cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                       int grid, cudaStream_t s) {
-  return launch_gemm<true>(tmA, tmB, p, grid, s);
+cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                       const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm<true>(tmA, tmB, tmS, p, grid, s);
 }
 
-cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                       int grid, cudaStream_t s) {
-  return launch_gemm<false>(tmA, tmB, p, grid, s);
+cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                       const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm<false>(tmA, tmB, tmS, p, grid, s);
 }
 
 }  // namespace moe

@@ -1,0 +1,443 @@
+// Small-batch grouped FP8 x FP8 GEMM: weight rows on the MMA's M side, up to 32 tokens on N.
+//
+// (TensorRT-LLM "Triton FP8-activation MoE for decode-sized batches on Hopper", description: at
+// decode sizes the grid should cover only the expert blocks the batch occupies and stream the FP8
+// weights at the bandwidth bound; vLLM "Skip padded work in block-FP8 DeepGemmExperts", Purpose:
+// only live (expert, rows) work is visited.)
+//
+// At decode sizes an expert holds a handful of rows, so a 128-row tile wastes the tensor-memory
+// lanes and makes the per-128-K promotion read 128 x 256 partial sums for a few live rows.  Here the
+// work item is a live 32-row chunk of one expert (from the alignment kernel's chunk list) x one
+// output block x one K split:
+//   warp 0 (one lane)  TMA producer: per 128-wide K block one stage of a 5-stage ring receives 2 x 128
+//                      weight rows (FC1: gate block and the matching up block; FC2: two 128-column
+//                      blocks of H), the chunk's live activation rows (8-row boxes), the chunk's 32
+//                      activation scales and the two weight block scales.
+//   warp 1 (one lane)  MMA issuer: per K block 2 x 4 tcgen05.mma kind::f8f6f4 with M = 128 weight
+//                      rows, N = 32 tokens, K = 32, into one of four 64-column accumulators.
+//   warps 2..9         promotion + epilogue.  Warp (q, half) owns weight rows 32q..32q+31 (its TMEM
+//                      lane quarter) and tokens 16*half..16*half+15: per K block two 16-column
+//                      tensor-memory loads and acc += partial * (a_scale[token] * w_scale).
+// The epilogue is spread over all 256 threads: FC1 thread j applies SwiGLU to its (gate j, up j)
+// for each live token, the 1x128 amax of a token is a shuffle + shared-memory reduction over the
+// 128 lanes, and each warp writes 32 consecutive FP8 codes per token.  FC2 threads write BF16 y.
+// K splits (FC1): each split publishes fp32 partials per pair; the last split to arrive sums them
+// in split order and runs the epilogue.
+#include "moe_device.cuh"
+
+namespace moe {
+
+constexpr int kSN = 32;                       // tokens per chunk (MMA N)
+constexpr int kSStages = 5;
+constexpr int kSWBytes = 2 * kGroup * kBK;    // 256 weight rows x 128 bytes
+constexpr int kSXBytes = kSN * kBK;           // 32 token rows x 128 bytes
+constexpr int kSStageBytes = kSWBytes + kSXBytes;
+constexpr int kSSlotBytes = 384;              // [0,128) act scales, [128,144) w0, [256,272) w1
+constexpr int kSSlotW0 = 128;
+constexpr int kSSlotW1 = 256;
+constexpr int kSTmemBufs = 4;
+constexpr int kSBufCols = 2 * kSN;            // gate/up (or block 0/1) x 32 tokens
+constexpr int kSTmemCols = kSTmemBufs * kSBufCols;
+constexpr int kSThreads = 320;
+constexpr int kSSmemBytes = kSStages * (kSStageBytes + kSSlotBytes) + 1024 /*align*/ +
+                            1024 /*bars*/ + 2 * 4 * kSN * 4 /*token amax exchange*/;
+constexpr uint32_t kSIdesc = make_idesc_e4m3(kGroup, kSN);
+
+struct Chunk {
+  int chunk, nb, ks, e, row0, live;
+};
+
+__device__ __forceinline__ Chunk decode_chunk(const GemmParams& p, int item) {
+  Chunk c;
+  const int per = p.n_blocks * p.ksplit;
+  c.chunk = item / per;
+  const int rem = item - c.chunk * per;
+  c.nb = rem / p.ksplit;
+  c.ks = rem - c.nb * p.ksplit;
+  c.row0 = p.chunk_row0[c.chunk];
+  c.e = p.tile_expert[c.row0 / kAlign];
+  c.live = min(kSN, p.live_end[c.e] - c.row0);
+  return c;
+}
+
+__device__ __forceinline__ float s_swiglu(float g, float u, int mode, float lim) {
+  if (mode == MOE_CLAMP_BEFORE_SILU) {
+    g = fminf(g, lim);
+    u = fminf(fmaxf(u, -lim), lim);
+  }
+  const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-g)));   // correctly rounded 1/(1+e^-g)
+  float silu = __fmul_rn(g, sig);
+  if (mode == MOE_CLAMP_AFTER_SILU) {
+    silu = fminf(silu, lim);
+    u = fminf(fmaxf(u, -lim), lim);
+  }
+  return __fmul_rn(silu, u);
+}
+
+__device__ __forceinline__ void s_drain_wait(uint32_t bar, uint32_t parity, int* status) {
+  const uint64_t t0 = global_timer_ns();
+  while (!mbar_try_wait(bar, parity)) {
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicCAS(status, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+}
+
+template <bool kFC1>
+__global__ void __launch_bounds__(kSThreads, 1)
+    k_small_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                 const __grid_constant__ CUtensorMap tmS, const GemmParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw_base = smem_addr(smem_raw);
+  const uint32_t sbase = (raw_base + 1023u) & ~1023u;
+  uint8_t* smem = smem_raw + (sbase - raw_base);
+  uint8_t* slots = smem + kSStages * kSStageBytes;
+  uint8_t* ctrl = slots + kSStages * kSSlotBytes;
+  const uint32_t slot0 = smem_addr(slots);
+  const uint32_t bar0 = smem_addr(ctrl);
+  auto full_bar = [&](int s) { return bar0 + 8u * s; };
+  auto empty_bar = [&](int s) { return bar0 + 8u * (kSStages + s); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kSStages + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kSStages + kSTmemBufs + b); };
+  const uint32_t drain_bar = bar0 + 8u * (2 * kSStages + 2 * kSTmemBufs);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kSStages + 2 * kSTmemBufs + 1));
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* mma_consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
+  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
+  float* red = reinterpret_cast<float*>(ctrl + 1024);   // [2 halves][4 quarters][16 tokens]
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr int kEpiWarps = 8;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kSStages; ++s) {
+      mbar_init(full_bar(s), 1);
+      mbar_init(empty_bar(s), 1 + kEpiWarps);
+    }
+    for (int b = 0; b < kSTmemBufs; ++b) {
+      mbar_init(tfull_bar(b), 1);
+      mbar_init(tempty_bar(b), kEpiWarps);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    *mma_consumed = 0;
+    *last_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmA);
+    prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmS);
+  }
+  if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kSTmemCols);
+  tc_fence_before_sync();
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_slot;
+  grid_dep_wait();                 // the previous kernel's outputs are complete from here on
+  grid_dep_launch_dependents();
+
+  const int total = *p.num_chunks * p.n_blocks * p.ksplit;
+  const int KB = p.K / kBK;
+  const int kb_per_split = KB / p.ksplit;
+  const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
+  const int a_scale_bytes = a_ue ? kSN : kSN * 4;
+  const int w_per16 = b_ue ? 16 : 4;
+  const int ncb = p.b_rows_per_expert / kGroup;
+  int* status = p.status;
+
+  int prod_issued = 0;
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ producer
+    int it = 0;
+    bool ok = true;
+    const uint64_t pol_w = policy_evict_first();
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      const Chunk w = decode_chunk(p, item);
+      const int nbox = (w.live + kABoxRows - 1) / kABoxRows;
+      int brow0, brow1, sr0, sr1;
+      bool second;
+      if (kFC1) {
+        brow0 = w.e * p.b_rows_per_expert + w.nb * kGroup;
+        brow1 = brow0 + p.out_cols;
+        sr0 = w.e * ncb + w.nb;
+        sr1 = w.e * ncb + p.out_cols / kGroup + w.nb;
+        second = true;
+      } else {
+        brow0 = w.e * p.b_rows_per_expert + w.nb * 2 * kGroup;
+        brow1 = brow0 + kGroup;
+        sr0 = w.e * ncb + 2 * w.nb;
+        sr1 = sr0 + 1;
+        second = 2 * w.nb + 1 < ncb;
+      }
+      const uint32_t bytes = (second ? 2 : 1) * (kGroup * kBK) + nbox * (kABoxRows * kBK) +
+                             a_scale_bytes + (second ? 32 : 16);
+      const int kb0 = w.ks * kb_per_split;
+      for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
+        const int s = it % kSStages;
+        const uint32_t ph = (it / kSStages) & 1;
+        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(full_bar(s), bytes);
+        const uint32_t sW = sbase + s * kSStageBytes;
+        const uint32_t sX = sW + kSWBytes;
+        const uint32_t sS = slot0 + s * kSSlotBytes;
+        tma_load_2d_hint(sW, &tmB, kb * kBK, brow0, full_bar(s), pol_w);
+        if (second) tma_load_2d_hint(sW + kGroup * kBK, &tmB, kb * kBK, brow1, full_bar(s), pol_w);
+        for (int j = 0; j < nbox; ++j)
+          tma_load_2d(sX + j * (kABoxRows * kBK), &tmA, kb * kBK, w.row0 + j * kABoxRows, full_bar(s));
+        bulk_copy_g2s(sS, static_cast<const uint8_t*>(p.a_scale) +
+                              ((size_t)kb * p.R_cap + w.row0) * (a_ue ? 1 : 4),
+                      a_scale_bytes, full_bar(s));
+        const int i0 = sr0 * KB + kb;
+        tma_load_1d(sS + kSSlotW0, &tmS, i0 - i0 % w_per16, full_bar(s));
+        if (second) {
+          const int i1 = sr1 * KB + kb;
+          tma_load_1d(sS + kSSlotW1, &tmS, i1 - i1 % w_per16, full_bar(s));
+        }
+        ++it;
+      }
+    }
+    prod_issued = it;
+  } else if (warp == 1 && lane == 0) {
+    // ---------------------------------------------------------------- MMA
+    int it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      for (int k = 0; k < kb_per_split; ++k) {
+        const int s = it % kSStages;
+        const int b = it % kSTmemBufs;
+        if (!mbar_wait(full_bar(s), (it / kSStages) & 1, abort_flag, status) ||
+            !mbar_wait(tempty_bar(b), ((it / kSTmemBufs) & 1) ^ 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const uint32_t sW = sbase + s * kSStageBytes;
+        const uint64_t xdesc = make_sdesc_sw128(sW + kSWBytes);
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t d = tmem_base + b * kSBufCols + h * kSN;
+          const uint64_t wdesc = make_sdesc_sw128(sW + h * (kGroup * kBK));
+#pragma unroll
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_f8(d, wdesc + 2 * kk, xdesc + 2 * kk, kSIdesc, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(empty_bar(s));
+        mma_commit(tfull_bar(b));
+        ++it;
+        *mma_consumed = it;
+      }
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ---------------------------------------------------- promotion + epilogue
+    const int ew = warp - kEpiWarp0;
+    const int half = ew >> 2;            // tokens 16*half .. 16*half + 15
+    const int q = warp & 3;              // weight rows 32q .. 32q + 31 (TMEM lane quarter)
+    const int j = q * 32 + lane;         // weight row (output column) inside the 128 block
+    const uint32_t hb = (uint32_t)(half * 16);
+    int it = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      const Chunk w = decode_chunk(p, item);
+      const int ntok = max(0, min(16, w.live - half * 16));   // live tokens of this half
+      int sr0, sr1;
+      bool has1;
+      if (kFC1) {
+        sr0 = w.e * ncb + w.nb;
+        sr1 = w.e * ncb + p.out_cols / kGroup + w.nb;
+        has1 = true;
+      } else {
+        sr0 = w.e * ncb + 2 * w.nb;
+        sr1 = sr0 + 1;
+        has1 = 2 * w.nb + 1 < ncb;
+      }
+      float acc0[16], acc1[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) acc0[c] = acc1[c] = 0.0f;
+      const int kb0 = w.ks * kb_per_split;
+      for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
+        const int s = it % kSStages;
+        const int b = it % kSTmemBufs;
+        if (!mbar_wait(tfull_bar(b), (it / kSTmemBufs) & 1, abort_flag, status) ||
+            !mbar_wait(full_bar(s), (it / kSStages) & 1, abort_flag, status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        if (ntok > 0) {
+          const uint8_t* slot = slots + s * kSSlotBytes;
+          const int i0 = sr0 * KB + kb, i1 = sr1 * KB + kb;
+          const float sw0 = smem_scale_at(slot + kSSlotW0, i0 % w_per16, b_ue);
+          const float sw1 = has1 ? smem_scale_at(slot + kSSlotW1, i1 % w_per16, b_ue) : 0.0f;
+          uint32_t r0[16], r1[16];
+          const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kSBufCols + hb;
+          tmem_ld16(t0, r0);
+          tmem_ld16(t0 + kSN, r1);
+          float sa[16];
+#pragma unroll
+          for (int c = 0; c < 16; ++c) sa[c] = smem_scale_at(slot, half * 16 + c, a_ue);
+          tmem_ld_wait();
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            acc0[c] = fmaf(__uint_as_float(r0[c]), __fmul_rn(sa[c], sw0), acc0[c]);
+            acc1[c] = fmaf(__uint_as_float(r1[c]), __fmul_rn(sa[c], sw1), acc1[c]);
+          }
+        }
+        tc_fence_before_sync();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(empty_bar(s));
+          mbar_arrive(tempty_bar(b));
+        }
+        ++it;
+      }
+      if (!ok) break;
+
+      if (kFC1) {
+        const int I = p.out_cols;
+        if (p.ksplit > 1) {
+          // split-K fix-up over pairs: partial[ks][pair][2I], the last split sums in split order
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c < ntok) {
+              const int pair = p.sorted_pair[w.row0 + half * 16 + c];
+              float* dst = p.splitk_partial + ((size_t)w.ks * p.P_cap + pair) * (2 * I);
+              dst[w.nb * kGroup + j] = acc0[c];
+              dst[I + w.nb * kGroup + j] = acc1[c];
+            }
+          }
+          __threadfence();
+          named_barrier_sync(1, 256);
+          if (ew == 0 && lane == 0) {
+            const int prev = atomicAdd(&p.splitk_count[w.chunk * p.n_blocks + w.nb], 1);
+            *last_flag = (prev == p.ksplit - 1);
+          }
+          named_barrier_sync(1, 256);
+          const bool last = *last_flag != 0;
+          named_barrier_sync(1, 256);
+          if (!last) continue;
+          __threadfence();
+          if (ew == 0 && lane == 0) p.splitk_count[w.chunk * p.n_blocks + w.nb] = 0;
+#pragma unroll
+          for (int c = 0; c < 16; ++c) {
+            if (c < ntok) {
+              const int pair = p.sorted_pair[w.row0 + half * 16 + c];
+              // issue every split's load first (one round trip), then sum in split order
+              float gv[kMaxKSplit], uv[kMaxKSplit];
+#pragma unroll
+              for (int s = 0; s < kMaxKSplit; ++s) {
+                if (s < p.ksplit) {
+                  const float* src = p.splitk_partial + ((size_t)s * p.P_cap + pair) * (2 * I);
+                  gv[s] = __ldcg(src + w.nb * kGroup + j);
+                  uv[s] = __ldcg(src + I + w.nb * kGroup + j);
+                }
+              }
+              float g = 0.0f, u = 0.0f;
+#pragma unroll
+              for (int s = 0; s < kMaxKSplit; ++s) {
+                if (s < p.ksplit) {
+                  g = __fadd_rn(g, gv[s]);
+                  u = __fadd_rn(u, uv[s]);
+                }
+              }
+              acc0[c] = g;
+              acc1[c] = u;
+            }
+          }
+        }
+        // SwiGLU per (j, token), then the token's 1x128 amax over the 128 lanes j
+        float* r = red + half * (4 * 16);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c < ntok) {
+            const float h = s_swiglu(bf16_round(acc0[c]), bf16_round(acc1[c]), p.clamp_mode,
+                                     p.clamp_limit);
+            acc0[c] = h;
+            float m = fabsf(h);
+#pragma unroll
+            for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+            if (lane == 0) r[q * 16 + c] = m;
+          }
+        }
+        named_barrier_sync(2 + half, 128);
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c < ntok) {
+            const float amax = fmaxf(fmaxf(r[c], r[16 + c]), fmaxf(r[32 + c], r[48 + c]));
+            const float s = group_scale(amax, p.act_fmt);
+            const int row = w.row0 + half * 16 + c;
+            p.a2_q[(size_t)row * I + w.nb * kGroup + j] =
+                (uint8_t)(cvt_e4m3x2(__fdiv_rn(acc0[c], s), 0.0f) & 0xFF);
+            if (j == 0)
+              store_scale(p.a2_s, (size_t)w.nb * p.R_cap + row, s, p.act_fmt == MOE_SCALE_UE8M0);
+          }
+        }
+        named_barrier_sync(2 + half, 128);
+      } else {
+#pragma unroll
+        for (int c = 0; c < 16; ++c) {
+          if (c < ntok) {
+            uint16_t* yrow = p.y + (size_t)(w.row0 + half * 16 + c) * p.out_cols + w.nb * 2 * kGroup;
+            yrow[j] = (uint16_t)f32_to_bf16_bits(acc0[c]);
+            if (has1) yrow[kGroup + j] = (uint16_t)f32_to_bf16_bits(acc1[c]);
+          }
+        }
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- teardown
+  __syncthreads();
+  if (warp == 1 && lane == 0) {
+    mma_commit(drain_bar);
+    s_drain_wait(drain_bar, 0, status);
+  }
+  if (warp == 0 && lane == 0 && *abort_flag) {
+    for (int it = *mma_consumed; it < prod_issued; ++it)
+      s_drain_wait(full_bar(it % kSStages), (it / kSStages) & 1, status);
+  }
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, kSTmemCols);
+  }
+}
+
+template <bool kFC1>
+static cudaError_t launch_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                                const GemmParams& p, int grid, cudaStream_t s) {
+  cudaError_t err = cudaFuncSetAttribute(k_small_gemm<kFC1>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kSSmemBytes);
+  if (err != cudaSuccess) return err;
+  return launch_pdl(k_small_gemm<kFC1>, dim3(grid), dim3(kSThreads), kSSmemBytes, s, tmA, tmB, tmS,
+                    p);
+}
+
+cudaError_t launch_fc1_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                             const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_small<true>(tmA, tmB, tmS, p, grid, s);
+}
+
+cudaError_t launch_fc2_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                             const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_small<false>(tmA, tmB, tmS, p, grid, s);
+}
+
+}  // namespace moe

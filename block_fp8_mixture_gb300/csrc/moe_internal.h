@@ -16,6 +16,7 @@ constexpr int kGroup = 128;               // 1x128 activation group = 128x128 we
 constexpr int kMaxExperts = 1024;
 constexpr int kMaxTopk = 16;
 constexpr int kMaxPairs = 1 << 20;
+constexpr int kMaxKSplit = 8;                      // largest FC1 K-split of the small-batch schedule
 constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s bound on any device-side wait
 constexpr float kScaleFloor = 1.0f / 229376.0f;    // 1/(448*512), rounded to fp32
 
@@ -26,7 +27,7 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;
 constexpr int kStages = 4;
-constexpr int kABoxRows = 32;                         // activation rows per TMA box
+constexpr int kABoxRows = 8;                          // activation rows per TMA box (one swizzle atom)
 constexpr int kABytes = kBM * kBK;                    // 16 KB
 constexpr int kBBytes = kBN * kBK;                    // 32 KB
 constexpr int kStageBytes = kABytes + kBBytes;
@@ -34,8 +35,13 @@ constexpr int kGemmThreads = 320;                     // TMA warp, MMA warp, 8 e
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiThreads = 256;
 constexpr int kTmemCols = 512;                        // two 256-column accumulators
-constexpr int kGemmSmemBytes = kStages * kStageBytes + 1024 /*align*/ + 1024 /*bars*/ +
-                               2 * kBM * 4 /*row amax exchange*/;
+// Per-stage scale slot: [0, 512) the 128 activation scales of the K block (fp32 or UE8M0 bytes),
+// [512, 528) and [640, 656) the 16-byte aligned chunks holding the two weight block scales.
+constexpr int kScaleSlotBytes = 768;
+constexpr int kSlotWScale0 = 512;
+constexpr int kSlotWScale1 = 640;
+constexpr int kGemmSmemBytes = kStages * kStageBytes + kStages * kScaleSlotBytes + 1024 /*align*/ +
+                               1024 /*bars*/ + 2 * kBM * 4 /*row amax exchange*/;
 
 struct Plan {
   moe_ws_plan ws;
@@ -59,6 +65,8 @@ struct AlignParams {
   int32_t* status;
   int32_t* splitk_count;
   int splitk_count_len;
+  int32_t* chunk_row0;
+  int32_t* num_chunks;
 };
 
 struct QuantParams {
@@ -95,6 +103,9 @@ struct GemmParams {
   int32_t* splitk_count;    // [T_cap * n_blocks]
   const int32_t* sorted_pair;
   int P_cap;
+  // small-batch schedule: live 32-row chunks
+  const int32_t* chunk_row0;
+  const int32_t* num_chunks;
   // FC2 epilogue
   uint16_t* y;
   int32_t* status;
@@ -109,12 +120,34 @@ struct ReduceParams {
   uint16_t* out;
 };
 
+// Launch with programmatic stream serialization: the kernel may start while the previous kernel of
+// the stream finishes; it orders itself with grid_dep_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 cudaError_t launch_align(const AlignParams& p, cudaStream_t s);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
-cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                       int grid, cudaStream_t s);
-cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const GemmParams& p,
-                       int grid, cudaStream_t s);
+cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                       const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                       const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_fc1_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                             const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_fc2_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
+                             const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t s);
 
 }  // namespace moe

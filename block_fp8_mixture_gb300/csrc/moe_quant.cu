@@ -23,6 +23,8 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant_act(QuantParams p) {
   const long gid = (long)blockIdx.x * kGroupsPerBlock + (threadIdx.x >> 4);
   const long t = gid / groups_per_row;
   const int g = (int)(gid % groups_per_row);
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   int n = p.M_cap;
   if (p.d_num_tokens != nullptr) n = min(max(*p.d_num_tokens, 0), p.M_cap);
   if (t >= n) return;   // the whole half-warp leaves together
@@ -58,8 +60,7 @@ cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
   const long groups = (long)p.M_cap * (p.H / kGroup);
   const long blocks = (groups + kGroupsPerBlock - 1) / kGroupsPerBlock;
   if (blocks == 0) return cudaSuccess;
-  k_quant_act<<<(unsigned)blocks, kQuantThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_quant_act, dim3((unsigned)blocks), dim3(kQuantThreads), 0, s, p);
 }
 
 // ----------------------------------------------------------------- reduce
@@ -71,6 +72,8 @@ constexpr int kReduceThreads = 128;
 
 __global__ void __launch_bounds__(kReduceThreads) k_topk_reduce(ReduceParams p) {
   const long t = blockIdx.x;
+  grid_dep_wait();
+  grid_dep_launch_dependents();
   int n = p.M_cap;
   if (p.d_num_tokens != nullptr) n = min(max(*p.d_num_tokens, 0), p.M_cap);
   if (t >= n) return;
@@ -101,8 +104,7 @@ __global__ void __launch_bounds__(kReduceThreads) k_topk_reduce(ReduceParams p) 
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t s) {
   if (p.M_cap == 0) return cudaSuccess;
   dim3 grid(p.M_cap, (p.H / 8 + kReduceThreads - 1) / kReduceThreads);
-  k_topk_reduce<<<grid, kReduceThreads, 0, s>>>(p);
-  return cudaGetLastError();
+  return launch_pdl(k_topk_reduce, grid, dim3(kReduceThreads), 0, s, p);
 }
 
 }  // namespace moe

@@ -68,7 +68,7 @@ SCALE_FLOOR = F32(1.0) / F32(448.0 * 512.0)   # RN32(1/229376)
 
 
 # ---------------------------------------------------------------- alignment
-def align(topk_ids, n_tokens, num_experts, align_to=ALIGN):
+def align(topk_ids, n_tokens, num_experts, align_to=ALIGN, chunk_rows=32):
     """Routing alignment into per-expert prefix-sum endpoints.
 
     Pairs p = t*topk + j for t < n_tokens; a pair is valid when its id is in
@@ -83,7 +83,8 @@ def align(topk_ids, n_tokens, num_experts, align_to=ALIGN):
     Returns a dict of int32 arrays: seg_start[E+1], live_end[E],
     pair_row[n*topk] (row of each pair, -1 when dropped), sorted_pair[rows]
     (pair of each live row, -1 on padding rows), tile_expert[num_tiles],
-    num_tiles.
+    num_tiles, and the small-batch work list: chunk_row0 = the first row of each
+    chunk_rows-row piece of every expert's live rows (experts ascending), num_chunks.
     """
     topk_ids = np.asarray(topk_ids, np.int64)
     topk = topk_ids.shape[1]
@@ -107,7 +108,12 @@ def align(topk_ids, n_tokens, num_experts, align_to=ALIGN):
     tile_expert = np.empty(num_tiles, np.int64)
     for e in range(num_experts):
         tile_expert[seg_start[e] // align_to: seg_start[e + 1] // align_to] = e
+    chunk_row0 = [int(seg_start[e]) + c * chunk_rows
+                  for e in range(num_experts)
+                  for c in range(-(-int(counts[e]) // chunk_rows))]
     return {
+        "chunk_row0": np.asarray(chunk_row0, np.int32),
+        "num_chunks": len(chunk_row0),
         "seg_start": seg_start.astype(np.int32),
         "live_end": live_end.astype(np.int32),
         "pair_row": pair_row.astype(np.int32),

@@ -50,7 +50,9 @@ def test_plan_sizes():
     assert p["y"] + p["R_cap"] * 4096 * 2 <= p["total_bytes"]
     assert moe.workspace_bytes(32, 288, 4096, 512, 8) == p["total_bytes"]
     # small batches split FC1's K; large ones do not
-    assert moe.workspace_plan(1, 288, 4096, 512, 8)["fc1_ksplit"] == 8
+    assert moe.workspace_plan(1, 288, 4096, 512, 8)["fc1_ksplit"] == 4
+    assert moe.workspace_plan(32, 288, 4096, 512, 8)["fc1_ksplit"] == 1
+    assert moe.workspace_plan(32, 288, 4096, 512, 8)["small_batch"] == 1
     assert moe.workspace_plan(4096, 32, 7168, 2048, 8)["fc1_ksplit"] == 1
     # UE8M0 scales take one byte
     p8 = moe.workspace_plan(32, 288, 4096, 512, 8, moe.SCALE_UE8M0)

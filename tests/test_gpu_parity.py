@@ -61,6 +61,8 @@ def test_align_bit_exact(E, topk, M_cap, n, lo, hi):
     assert np.array_equal(v["pair_row"].cpu().numpy()[: n * topk], ref["pair_row"])
     nt = ref["num_tiles"]
     assert np.array_equal(v["tile_expert"].cpu().numpy()[:nt], ref["tile_expert"])
+    assert int(v["num_chunks"].item()) == ref["num_chunks"]
+    assert np.array_equal(v["chunk_row0"].cpu().numpy()[: ref["num_chunks"]], ref["chunk_row0"])
     sp = v["sorted_pair"].cpu().numpy()
     live = ref["sorted_pair"] >= 0
     assert np.array_equal(sp[: live.size][live], ref["sorted_pair"][live])

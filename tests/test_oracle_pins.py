@@ -266,6 +266,14 @@ def test_align_brute_force():
             assert seg[e] <= i * A < seg[e + 1]
         assert np.all(r["seg_start"] % A == 0)
         assert (r["live_end"] - r["seg_start"][:-1]).sum() == len(pairs)
+        # 32-row chunks cover every live row exactly once and never cross a segment
+        covered = []
+        for c0 in r["chunk_row0"]:
+            e = [ee for ee in range(E) if seg[ee] <= c0 < r["live_end"][ee]]
+            assert len(e) == 1 and (c0 - seg[e[0]]) % 32 == 0
+            covered += list(range(c0, min(c0 + 32, r["live_end"][e[0]])))
+        assert sorted(covered) == sorted(exp_rows.values())
+        assert r["num_chunks"] == len(r["chunk_row0"])
 
 
 def test_align_edge_cases():
