@@ -72,6 +72,7 @@ SIGNATURES = {
     "moe_fc2": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
     "moe_topk_reduce": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
     "moe_fp8_block_forward": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
+    "moe_fp8_block_forward_static": (_I, [_P(FwdArgs), _VP]),
     "moe_last_device_status": (_I, [_VP, _VP]),
     "moe_status_str": (ctypes.c_char_p, [_I]),
     "moe_version": (ctypes.c_char_p, []),
@@ -211,6 +212,16 @@ def topk_reduce(args: FwdArgs, workspace, stream=None):
 def forward(args: FwdArgs, workspace, stream=None):
     """The whole layer (moe_fp8_block_forward) on `stream` (default: torch's current stream)."""
     _run("moe_fp8_block_forward", args, workspace, stream)
+
+
+def forward_static(args: FwdArgs, stream=None):
+    """The whole layer without a caller workspace (moe_fp8_block_forward_static): for callers that
+    cannot allocate device memory; small layers only (workspace <= STATIC_SCRATCH_BYTES)."""
+    _check(load_library().moe_fp8_block_forward_static(ctypes.byref(args), _stream(stream)),
+           "moe_fp8_block_forward_static")
+
+
+STATIC_SCRATCH_BYTES = 32 << 20
 
 
 def last_device_status(workspace, stream=None) -> int:

@@ -172,6 +172,27 @@ moe_status moe_topk_reduce(const moe_fwd_args* args, void* workspace, size_t wor
 moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
                                  moe_stream_t stream);
 
+/* Size of the library-owned scratch array used by moe_fp8_block_forward_static (32 MiB). */
+#define MOE_STATIC_SCRATCH_BYTES (32u << 20)
+
+/* The whole layer without a caller workspace and without any allocation.  The pages have no
+ * counterpart: this is for callers that cannot allocate device memory when they run the layer (a
+ * runtime that owns a fixed memory arena, a latency-critical loop that must not risk the device
+ * synchronisation cudaMalloc/cudaFree can cause, plugin code that only receives input and output
+ * pointers).  Same arguments and results as moe_fp8_block_forward; the workspace is a fixed
+ * MOE_STATIC_SCRATCH_BYTES array inside the library, present on every GPU that loads the library
+ * until the process exits.
+ *  - Layers whose moe_workspace_bytes(...) exceeds MOE_STATIC_SCRATCH_BYTES are rejected with
+ *    MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched (e.g. single-token decode fits; the
+ *    32-token, 288-expert decode layer does not).
+ *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
+ *    that device current; make that first call before any stream capture.
+ *  - All calls on a device share the array and it keeps the last call's contents; the state that
+ *    must start at zero is reset on the GPU by every call.  Calls that overlap on the GPU (other
+ *    streams or host threads) race on the array: serialise them.
+ *  - The device status word of these calls is not readable through moe_last_device_status. */
+moe_status moe_fp8_block_forward_static(const moe_fwd_args* args, moe_stream_t stream);
+
 /* Reads the workspace status word (synchronizes `stream` first).  MOE_OK or MOE_ERR_DEVICE_TIMEOUT. */
 moe_status moe_last_device_status(const void* workspace, moe_stream_t stream);
 
