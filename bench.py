@@ -165,14 +165,22 @@ def ncu_traffic(key: str):
     return entry.get("dram_bytes_per_launch")
 
 
+FMT_NAMES = {0: "fp32", 1: "fp32-pow2", 2: "ue8m0"}
+
+
+def workload_name(shape, M, n):
+    live = f"M={M}" if n == M else f"capacity {M}, {n} live"
+    return f"{shape.name} MoE layer E={shape.E} H={shape.H} I={shape.I} top-{shape.topk} {live}"
+
+
 # ------------------------------------------------------------ our arm
-class DecodeBench:
-    def __init__(self, M, rank, weights, dev_weights):
+class LayerBench:
+    def __init__(self, workload, M, n, rank, weights, dev_weights):
         import torch
         import block_fp8_mixture_gb300 as moe
         self.moe = moe
         self.M = M
-        self.case = synth.make_case(WORKLOAD, M, seed=2000 + M + 7919 * rank, weights=weights)
+        self.case = synth.make_case(workload, M, n, seed=2000 + M + 7919 * rank, weights=weights)
         sh = self.case.shape
         self.sh = sh
         self.x = torch.from_numpy(self.case.x_bits.view(np.int16)).cuda().view(torch.bfloat16)
@@ -183,7 +191,8 @@ class DecodeBench:
                                   act_fmt=sh.act_fmt, clamp_mode=sh.clamp_mode,
                                   clamp_limit=sh.limit, max_tokens=M, topk=sh.topk)
         self.out = torch.empty((M, sh.H), dtype=torch.bfloat16, device="cuda")
-        self.args = self.layer.args(self.x, self.ids, self.wts, self.out)
+        self.d_n = torch.tensor([self.case.n], dtype=torch.int32, device="cuda")
+        self.args = self.layer.args(self.x, self.ids, self.wts, self.out, d_num_tokens=self.d_n)
         self.ws = self.layer.workspace
 
     def forward(self, stream):
@@ -193,8 +202,10 @@ class DecodeBench:
         """The five steps as separate C-ABI calls (same kernels as forward())."""
         moe, sh, ws = self.moe, self.sh, self.ws
         return [
-            lambda: moe.align(self.ids, sh.E, sh.H, sh.I, ws, act_fmt=sh.act_fmt, stream=stream),
-            lambda: moe.quant_act(self.x, sh.topk, sh.E, sh.I, ws, act_fmt=sh.act_fmt, stream=stream),
+            lambda: moe.align(self.ids, sh.E, sh.H, sh.I, ws, d_num_tokens=self.d_n, act_fmt=sh.act_fmt,
+                              stream=stream),
+            lambda: moe.quant_act(self.x, sh.topk, sh.E, sh.I, ws, d_num_tokens=self.d_n,
+                                  act_fmt=sh.act_fmt, stream=stream),
             lambda: moe.fc1_swiglu_quant(self.args, ws, stream),
             lambda: moe.fc2(self.args, ws, stream),
             lambda: moe.topk_reduce(self.args, ws, stream),
@@ -212,13 +223,15 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     peaks = load_peaks()
-    shape = synth.SHAPES[WORKLOAD]
+    shape = synth.SHAPES[args.workload]
     weights = synth.make_weights(shape)
     dev_w = tuple(torch.from_numpy(a).cuda() for a in (weights.w13, weights.s13, weights.w2, weights.s2))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
-    sweep = sorted(set(SWEEP_M) | {args.M}) if not (args.no_sweep or args.profile_run) else [args.M]
-    benches = {M: DecodeBench(M, rank, weights, dev_w) for M in sweep}
+    do_sweep = args.workload == WORKLOAD and not (args.no_sweep or args.profile_run)
+    sweep = sorted(set(SWEEP_M) | {args.M}) if do_sweep else [args.M]
+    benches = {M: LayerBench(args.workload, M, args.n if M == args.M else M, rank, weights, dev_w)
+               for M in sweep}
 
     # graphs of the whole forward, one per M
     graphs = {}
@@ -327,12 +340,22 @@ def run_ours(args, rank, world):
     kern = per_kernel(args.M, max(10, min(args.steps, 50)))
     fc1_us = kern["fc1"]
     hbm_peak = peaks["hbm_gbs"]
-    fc1_gbs = work["fc1_bytes"] / (fc1_us * 1e-6) / 1e9
-    traffic = ncu_traffic(f"fc1_decode_M{args.M}")
-    roofline = {"kernel": "fc1 (grouped GEMM + SwiGLU + requant)", "bound": "hbm",
-                "achieved": fc1_gbs, "peak": hbm_peak, "unit": "GB/s", "frac": fc1_gbs / hbm_peak,
-                "traffic": traffic, "algorithmic_bytes": work["fc1_bytes"],
-                "avg_launch_us": fc1_us, "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)"}
+    fp8_peak = fp8_peak_tflops(peaks)
+    traffic = ncu_traffic(f"fc1_{args.workload}_M{args.M}")
+    if work["fc1_flops"] / (fp8_peak * 1e12) > work["fc1_bytes"] / (hbm_peak * 1e9):
+        achieved = work["fc1_flops"] / (fc1_us * 1e-6) / 1e12
+        roofline = {"kernel": "fc1 (grouped GEMM + SwiGLU + requant)", "bound": "tensor",
+                    "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
+                    "frac": achieved / fp8_peak, "traffic": traffic,
+                    "algorithmic_flops": work["fc1_flops"], "avg_launch_us": fc1_us,
+                    "peak_source": f"{peaks['source']}: 2 x MEASURED_PEAKS bf16_tflops (dense FP8 = 2x BF16)"}
+    else:
+        achieved = work["fc1_bytes"] / (fc1_us * 1e-6) / 1e9
+        roofline = {"kernel": "fc1 (grouped GEMM + SwiGLU + requant)", "bound": "hbm",
+                    "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                    "frac": achieved / hbm_peak, "traffic": traffic,
+                    "algorithmic_bytes": work["fc1_bytes"], "avg_launch_us": fc1_us,
+                    "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)"}
 
     def layer_roof(M, t_us):
         w = layer_work(benches[M].case)
@@ -357,8 +380,10 @@ def run_ours(args, rank, world):
         "metric": METRIC, "value": us_mean, "unit": "us", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us_mean / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-        "config": {"workload": f"decode MoE layer E=288 H=4096 I=512 top-8 M={args.M}",
-                   "clamp": "SwiGLU clamp 7.0 before SiLU", "scales": "fp32 128x128 weight, fp32 1x128 act",
+        "config": {"workload": workload_name(shape, args.M, args.n),
+                   "clamp": ("none" if shape.clamp_mode == 0 else
+                             f"SwiGLU clamp {shape.limit} {'before' if shape.clamp_mode == 1 else 'after'} SiLU"),
+                   "scales": f"weights {FMT_NAMES[shape.weight_fmt]} 128x128, activations {FMT_NAMES[shape.act_fmt]} 1x128",
                    "l2": "flushed before every step (512 MB write)", "timing": "CUDA graph replay, CUDA events",
                    "parallelism": f"replicas x{world}"},
         "roofline": roofline,
@@ -441,13 +466,20 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
-    ap.add_argument("--M", type=int, default=32, help="live tokens of the headline point")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.SHAPES),
+                    help="layer shape (default: the decode layer the metric is quoted on)")
+    ap.add_argument("--M", type=int, default=None, help="token capacity of the headline point")
+    ap.add_argument("--n", type=int, default=None, help="live tokens (default: M)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-run", action="store_true",
                     help="only W + K graph replays of the headline point (for ncu captures)")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
+    if args.M is None:
+        args.M = {"decode": 32, "tiny": 16}.get(args.workload, 4096)
+    if args.n is None:
+        args.n = args.M
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":

@@ -40,10 +40,11 @@ class MoeError(RuntimeError):
 class WsPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "num_tiles", "seg_start", "live_end", "sorted_pair", "pair_row", "tile_expert",
-        "num_chunks", "chunk_row0", "a1_q", "a1_s", "a2_q", "a2_s", "y", "splitk_partial",
+        "num_chunks", "chunk_row0", "align_hist", "a1_q", "a1_s", "a2_q", "a2_s", "y", "splitk_partial",
         "splitk_count", "total_bytes")] + [
         ("R_cap", ctypes.c_int32), ("T_cap", ctypes.c_int32), ("C_cap", ctypes.c_int32),
-        ("P_cap", ctypes.c_int32), ("fc1_ksplit", ctypes.c_int32), ("small_batch", ctypes.c_int32)]
+        ("P_cap", ctypes.c_int32), ("fc1_ksplit", ctypes.c_int32), ("small_batch", ctypes.c_int32),
+        ("align_ctas", ctypes.c_int32)]
 
     def as_dict(self):
         return {name: getattr(self, name) for name, _ in self._fields_}

@@ -1,20 +1,24 @@
-// Routing alignment into per-expert prefix-sum endpoints, one CTA.
+// Routing alignment into per-expert prefix-sum endpoints.
 //
 // (vLLM "Skip padded work in block-FP8 DeepGemmExperts", Purpose: the permutation helper produces
 // the expert endpoints both grouped GEMMs and the fused activation quantization consume;
 // TensorRT-LLM "Triton FP8-activation MoE for decode-sized batches on Hopper", description: one
 // program aligns the routed pairs.)
 //
-// A stable counting sort of the valid pairs p = t*k + j (t < n) by expert.  The 32 warps of the CTA
-// each own a contiguous range of pairs:
-//   pass 1  each warp counts its range per expert (warp-private histogram row, no atomics:
+// A stable counting sort of the valid pairs p = t*k + j (t < n) by expert.  The pairs are cut into
+// G contiguous ranges, one per CTA (G = 1 for small batches).  Inside a CTA the 32 warps each own a
+// contiguous sub-range:
+//   pass 1  each warp counts its sub-range per expert (warp-private histogram row, no atomics:
 //           __match_any_sync groups equal ids, the group leader adds the group size);
-//   scan    per expert, exclusive prefix over the warps' counts (gives each warp its base inside
-//           the expert) and a CTA-wide exclusive scan of the 128-padded counts (segment starts);
-//   pass 2  each warp walks its range again in order and places every pair at
-//           seg_start[e] + warp base + rank among the earlier equal ids of its 32-pair chunk.
-// Ascending pair order inside a segment follows because warps own ascending ranges and chunks are
-// visited in order.
+//   counts  per expert, exclusive prefix over the warps (each warp's base inside the CTA's share)
+//           and, for G > 1, over the CTAs' counts written by k_align_count (the CTA's base inside
+//           the expert);
+//   scan    CTA-wide exclusive scans of the 128-padded counts (segment starts) and of the 32-row
+//           chunk counts (small-batch work list); every CTA computes them, CTA 0 writes them;
+//   pass 2  each warp walks its sub-range again in order and places every pair at
+//           seg_start[e] + CTA base + warp base + rank among the earlier equal ids of its 32 pairs.
+// Ascending pair order inside a segment follows because CTAs and warps own ascending ranges and
+// chunks of 32 pairs are visited in order.
 #include "moe_device.cuh"
 
 namespace moe {
@@ -50,11 +54,45 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int* 
   return excl;
 }
 
+__device__ __forceinline__ int live_pairs(const AlignParams& p) {
+  int n = p.M_cap;
+  if (p.d_num_tokens != nullptr) n = min(max(*p.d_num_tokens, 0), p.M_cap);
+  return n * p.topk;
+}
+
+__device__ __forceinline__ void reset_shared_state(const AlignParams& p) {
+  if (threadIdx.x == 0) *p.status = 0;
+  for (int i = threadIdx.x; i < p.splitk_count_len; i += kAlignThreads) p.splitk_count[i] = 0;
+}
+
+// Large batches, step 1: expert counts of each CTA's range of pairs.
+__global__ void __launch_bounds__(kAlignThreads, 1) k_align_count(AlignParams p) {
+  extern __shared__ int32_t hist[];   // [E]
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  const int E = p.E;
+  const int num_pairs = live_pairs(p);
+  if (blockIdx.x == 0) reset_shared_state(p);
+  for (int e = threadIdx.x; e < E; e += kAlignThreads) hist[e] = 0;
+  __syncthreads();
+  const int per = (num_pairs + gridDim.x - 1) / gridDim.x;
+  const int begin = min((int)blockIdx.x * per, num_pairs);
+  const int end = min(begin + per, num_pairs);
+  for (int i = begin + threadIdx.x; i < end; i += kAlignThreads) {
+    const int id = p.topk_ids[i];
+    if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += kAlignThreads) p.cta_hist[blockIdx.x * E + e] = hist[e];
+}
+
+// The placement (and, for one CTA, the whole alignment).
 __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
   extern __shared__ int32_t sm[];
   const int E = p.E;
   int32_t* hist = sm;                              // [32][E]
   int32_t* seg = sm + kAlignWarps * E;             // [E + 1]
+  int32_t* base = seg + E + 1;                     // [E]: this CTA's first rank inside each expert
   __shared__ int32_t warp_sums[kAlignWarps];
 
   const int tid = threadIdx.x;
@@ -64,22 +102,22 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
 
   grid_dep_wait();
   grid_dep_launch_dependents();
-  int n = p.M_cap;
-  if (p.d_num_tokens != nullptr) n = min(max(*p.d_num_tokens, 0), p.M_cap);
-  const int num_pairs = n * p.topk;
-
-  if (tid == 0) *p.status = 0;
-  for (int i = tid; i < p.splitk_count_len; i += kAlignThreads) p.splitk_count[i] = 0;
+  const int num_pairs = live_pairs(p);
+  const int G = p.num_ctas;
+  if (G == 1) reset_shared_state(p);
   for (int i = tid; i < kAlignWarps * E; i += kAlignThreads) hist[i] = 0;
   __syncthreads();
 
-  const int chunk = (num_pairs + kAlignWarps - 1) / kAlignWarps;
-  const int begin = min(warp * chunk, num_pairs);
-  const int end = min(begin + chunk, num_pairs);
+  const int per_cta = (num_pairs + G - 1) / G;
+  const int cbegin = min((int)blockIdx.x * per_cta, num_pairs);
+  const int cend = min(cbegin + per_cta, num_pairs);
+  const int chunk = (cend - cbegin + kAlignWarps - 1) / kAlignWarps;
+  const int begin = min(cbegin + warp * chunk, cend);
+  const int end = min(begin + chunk, cend);
 
   // pass 1: per-warp histogram
-  for (int base = begin; base < end; base += 32) {
-    const int pi = base + lane;
+  for (int b0 = begin; b0 < end; b0 += 32) {
+    const int pi = b0 + lane;
     int e = -1;
     if (pi < end) {
       const int id = p.topk_ids[pi];
@@ -92,8 +130,8 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
   }
   __syncthreads();
 
-  // per-expert prefix over warps; padded count of expert e kept for the scan
-  int padded = 0;
+  // per-expert prefix over warps; expert totals and this CTA's base
+  int padded = 0, count = 0;
   for (int e = tid; e < E; e += kAlignThreads) {
     int run = 0;
     for (int w = 0; w < kAlignWarps; ++w) {
@@ -101,39 +139,50 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
       hist[w * E + e] = run;
       run += c;
     }
-    seg[e] = run;                                  // count, replaced by the start below
-    padded = (run + kAlign - 1) / kAlign * kAlign;
+    int before = 0, total = run;
+    if (G > 1) {
+      total = 0;
+      for (int g = 0; g < G; ++g) {
+        const int c = p.cta_hist[g * E + e];
+        if (g < (int)blockIdx.x) before += c;
+        total += c;
+      }
+    }
+    base[e] = before;
+    count = total;
+    padded = (total + kAlign - 1) / kAlign * kAlign;
   }
-  // exclusive scan of padded counts (E <= 1024 = one expert per thread)
-  int total = 0;
-  const int excl = block_exclusive_scan(padded, warp_sums, &total);
-  const int count = tid < E ? seg[tid] : 0;
-  // live 32-row chunks of each expert (the small-batch schedule's work list)
+  // exclusive scans over experts (E <= 1024 = one expert per thread)
+  int seg_total = 0;
+  const int excl = block_exclusive_scan(padded, warp_sums, &seg_total);
   int chunk_total = 0;
   const int chunk_base = block_exclusive_scan((count + kChunkRows - 1) / kChunkRows, warp_sums,
                                               &chunk_total);
-  if (tid < E) {
-    seg[tid] = excl;
-    p.seg_start[tid] = excl;
-    p.live_end[tid] = excl + count;
-    for (int c = 0; c * kChunkRows < count; ++c) p.chunk_row0[chunk_base + c] = excl + c * kChunkRows;
-  }
-  if (tid == 0) {
-    seg[E] = total;
-    p.seg_start[E] = total;
-    *p.num_tiles = total / kAlign;
-    *p.num_chunks = chunk_total;
+  if (tid < E) seg[tid] = excl;
+  if (tid == 0) seg[E] = seg_total;
+  if (blockIdx.x == 0) {
+    if (tid < E) {
+      p.seg_start[tid] = excl;
+      p.live_end[tid] = excl + count;
+      for (int c = 0; c * kChunkRows < count; ++c)
+        p.chunk_row0[chunk_base + c] = excl + c * kChunkRows;
+    }
+    if (tid == 0) {
+      p.seg_start[E] = seg_total;
+      *p.num_tiles = seg_total / kAlign;
+      *p.num_chunks = chunk_total;
+    }
   }
   __syncthreads();
-
-  // tile -> expert map
-  for (int e = tid; e < E; e += kAlignThreads) {
-    for (int t = seg[e] / kAlign; t < seg[e + 1] / kAlign; ++t) p.tile_expert[t] = e;
+  if (blockIdx.x == 0) {
+    // tile -> expert map
+    for (int e = tid; e < E; e += kAlignThreads)
+      for (int t = seg[e] / kAlign; t < seg[e + 1] / kAlign; ++t) p.tile_expert[t] = e;
   }
 
   // pass 2: stable placement
-  for (int base = begin; base < end; base += 32) {
-    const int pi = base + lane;
+  for (int b0 = begin; b0 < end; b0 += 32) {
+    const int pi = b0 + lane;
     int e = -1;
     if (pi < end) {
       const int id = p.topk_ids[pi];
@@ -143,7 +192,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
     const int rank = __popc(same & lanes_below);
     if (pi < end) {
       if (e >= 0) {
-        const int row = seg[e] + hist[warp * E + e] + rank;
+        const int row = seg[e] + base[e] + hist[warp * E + e] + rank;
         p.pair_row[pi] = row;
         p.sorted_pair[row] = pi;
       } else {
@@ -157,11 +206,17 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
 }
 
 cudaError_t launch_align(const AlignParams& p, cudaStream_t s) {
-  const size_t smem = (size_t)(kAlignWarps * p.E + p.E + 1) * sizeof(int32_t);
+  if (p.num_ctas > 1) {
+    const size_t csmem = (size_t)p.E * sizeof(int32_t);
+    const cudaError_t e0 =
+        launch_pdl(k_align_count, dim3(p.num_ctas), dim3(kAlignThreads), csmem, s, p);
+    if (e0 != cudaSuccess) return e0;
+  }
+  const size_t smem = (size_t)(kAlignWarps * p.E + 2 * p.E + 1) * sizeof(int32_t);
   cudaError_t err = cudaFuncSetAttribute(k_align, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          (int)smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_align, dim3(1), dim3(kAlignThreads), smem, s, p);
+  return launch_pdl(k_align, dim3(p.num_ctas), dim3(kAlignThreads), smem, s, p);
 }
 
 }  // namespace moe

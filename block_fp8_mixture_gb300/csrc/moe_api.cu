@@ -70,6 +70,8 @@ moe_status make_plan(int M_cap, int E, int H, int I, int topk, int act_fmt, Plan
   w.tile_expert = take((size_t)w.T_cap * 4);
   w.num_chunks = take(4);
   w.chunk_row0 = take((size_t)w.C_cap * 4);
+  w.align_ctas = P_cap > 4096 ? (int32_t)std::min<long long>(152, (P_cap + 1023) / 1024) : 1;
+  w.align_hist = take(w.align_ctas > 1 ? (size_t)w.align_ctas * E * 4 : 0);
   w.a1_q = take((size_t)R_cap * H);
   w.a1_s = take((size_t)(H / kGroup) * R_cap * sc);
   w.a2_q = take((size_t)R_cap * I);
@@ -120,6 +122,44 @@ static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Byte matrix [outer][inner] seen as 3-D (x = 128 bytes of a K block, y = row, z = K block), boxes of
+// box_outer rows x kPK K blocks: each row of a box is one kPK*128-byte contiguous run.
+static bool make_map_u8_3d_pk(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                              uint32_t box_outer, uint32_t pk) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)kBK, outer, inner / kBK};
+  const cuuint64_t strides[2] = {inner, (cuuint64_t)kBK};
+  const cuuint32_t box[3] = {(cuuint32_t)kBK, box_outer, pk};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// BF16 matrix [rows][cols] stored through 8-row x 64-column boxes with the 128-byte swizzle.
+static bool make_map_bf16_store(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {64, 8};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+static bool make_map_u8_3d_fc1(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                               uint32_t box_outer) {
+  return make_map_u8_3d_pk(m, base, inner, outer, box_outer, TileCfg<true>::PK);
+}
+
+static bool make_map_u8_3d_fc2(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
+                               uint32_t box_outer) {
+  return make_map_u8_3d_pk(m, base, inner, outer, box_outer, TileCfg<false>::PK);
 }
 
 // Flat array of n elements (fp32 or bytes), boxes of 16 bytes: used to fetch one block scale (and
@@ -212,6 +252,8 @@ static moe_status run_align(const int32_t* ids, const int32_t* d_n, const Plan& 
   p.splitk_count_len = pl.ws.fc1_ksplit > 1 ? pl.ws.C_cap * (pl.I / kGroup) : 0;
   p.chunk_row0 = at<int32_t>(ws, pl.ws.chunk_row0);
   p.num_chunks = at<int32_t>(ws, pl.ws.num_chunks);
+  p.cta_hist = at<int32_t>(ws, pl.ws.align_hist);
+  p.num_ctas = pl.ws.align_ctas;
   return launch_align(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -251,8 +293,10 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   if (pl.ws.R_cap == 0) return MOE_OK;
   CUtensorMap tmA, tmB, tmS;
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
-  if (!make_map_u8(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kABoxRows) ||
-      !make_map_u8(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup) ||
+  const bool small_maps = pl.ws.small_batch != 0;
+  auto mk = small_maps ? make_map_u8 : make_map_u8_3d_fc1;
+  if (!mk(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kABoxRows) ||
+      !mk(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup) ||
       !make_map_1d(&tmS, a->s13, w_ue, (uint64_t)pl.E * (2 * pl.I / kGroup) * (pl.H / kGroup)))
     return MOE_ERR_CUDA;
   GemmParams p;
@@ -283,8 +327,10 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   if (pl.ws.R_cap == 0) return MOE_OK;
   CUtensorMap tmA, tmB, tmS;
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
-  if (!make_map_u8(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kABoxRows) ||
-      !make_map_u8(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup) ||
+  const bool small_maps = pl.ws.small_batch != 0;
+  auto mk = small_maps ? make_map_u8 : make_map_u8_3d_fc2;
+  if (!mk(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kABoxRows) ||
+      !mk(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup) ||
       !make_map_1d(&tmS, a->s2, w_ue, (uint64_t)pl.E * (pl.H / kGroup) * (pl.I / kGroup)))
     return MOE_ERR_CUDA;
   GemmParams p;
@@ -301,8 +347,11 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   const bool small = pl.ws.small_batch != 0;
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
+  CUtensorMap tmY;
+  if (!small && !make_map_bf16_store(&tmY, at<void>(ws, pl.ws.y), pl.H, pl.ws.R_cap))
+    return MOE_ERR_CUDA;
   const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
-                                : launch_fc2(tmA, tmB, tmS, p, grid, s);
+                                : launch_fc2(tmA, tmB, tmS, tmY, p, grid, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

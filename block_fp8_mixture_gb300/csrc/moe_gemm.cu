@@ -33,7 +33,7 @@
 
 namespace moe {
 
-constexpr uint32_t kIdesc = make_idesc_e4m3(kBM, kBN);
+constexpr uint32_t kIdesc = make_idesc_e4m3(kBM, kGroup);   // M = 128, N = 128 per MMA
 
 struct Item {
   int tile, nb, ks, e, m0, live;
@@ -106,12 +106,21 @@ __device__ __forceinline__ void promote32(uint32_t taddr, float sab, float* acc)
 template <bool kFC1>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmS, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmY,
+                   const GemmParams p) {
+  using TC = TileCfg<kFC1>;
+  constexpr int kPK = TC::PK;
+  constexpr int kStages = TC::Stages;
+  constexpr int kStageBytes = TC::StageBytes;
+  constexpr int kABytes = TC::ABytes;
+  constexpr int kBHalfBytes = TC::BHalf;
+  constexpr int kScaleSlotBytes = TC::SlotBytes;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_base);
-  uint8_t* slots = smem + kStages * kStageBytes;               // scale slots, 1024-aligned
+  uint8_t* ystage = smem + kStages * kStageBytes;              // FC2 output staging, 1024-aligned
+  uint8_t* slots = ystage + 8 * TC::YWarpBytes;                 // scale slots, 128-byte aligned
   uint8_t* ctrl = slots + kStages * kScaleSlotBytes;
   const uint32_t slot0 = smem_addr(slots);
   const uint32_t bar0 = smem_addr(ctrl);
@@ -169,10 +178,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   const int w_per16 = b_ue ? 16 : 4;      // scale elements per 16-byte box
   int* status = p.status;
 
+  const int nst_item = (kb_per_split + kPK - 1) / kPK;   // pipeline stages per work item
   int prod_issued = 0;
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    int it = 0;
+    int sc = 0;
     bool ok = true;
     const uint64_t pol_w = policy_evict_first();
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
@@ -192,69 +202,87 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       int sr0, sr1;
       bool has_sr1;
       scale_rows<kFC1>(p, w, sr0, sr1, has_sr1);
-      const uint32_t bytes = nbox * (kABoxRows * kBK) + (second ? 2 : 1) * (kGroup * kBK) +
-                             a_scale_bytes + (has_sr1 ? 32 : 16);
-      const int kb0 = w.ks * kb_per_split;
-      for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
+      const int kb_end = (w.ks + 1) * kb_per_split;
+      for (int st = 0; st < nst_item; ++st) {
+        const int kbs = w.ks * kb_per_split + st * kPK;       // first K block of the stage
+        const int nv = min(kPK, kb_end - kbs);                // K blocks of the stage that exist
+        const int s = sc % kStages;
+        const uint32_t ph = (sc / kStages) & 1;
         if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) {
           ok = false;
           break;
         }
+        // boxes always deliver kPK K blocks (past the end of K they read as zero)
+        const uint32_t bytes = nbox * (kABoxRows * kBK * kPK) + (second ? 2 : 1) * kBHalfBytes +
+                               nv * (a_scale_bytes + (has_sr1 ? 32 : 16));
         mbar_arrive_expect_tx(full_bar(s), bytes);
         const uint32_t sA = sbase + s * kStageBytes;
         const uint32_t sB = sA + kABytes;
         const uint32_t sS = slot0 + s * kScaleSlotBytes;
+        // 8-row group j of the tile -> smem group 4*(j%4) + j/4, i.e. TMEM lanes 32*(j%4) + 8*(j/4)
         for (int j = 0; j < nbox; ++j)
-          tma_load_2d(sA + (32 * (j & 3) + 8 * (j >> 2)) * kBK, &tmA, kb * kBK,
-                      w.m0 + j * kABoxRows, full_bar(s));
-        tma_load_2d_hint(sB, &tmB, kb * kBK, brow0, full_bar(s), pol_w);
-        if (second) tma_load_2d_hint(sB + kGroup * kBK, &tmB, kb * kBK, brow1, full_bar(s), pol_w);
-        bulk_copy_g2s(sS, static_cast<const uint8_t*>(p.a_scale) +
-                              ((size_t)kb * p.R_cap + w.m0) * (a_ue ? 1 : 4),
-                      a_scale_bytes, full_bar(s));
-        const int i0 = sr0 * KB + kb;
-        tma_load_1d(sS + kSlotWScale0, &tmS, i0 - i0 % w_per16, full_bar(s));
-        if (has_sr1) {
-          const int i1 = sr1 * KB + kb;
-          tma_load_1d(sS + kSlotWScale1, &tmS, i1 - i1 % w_per16, full_bar(s));
+          tma_load_3d(sA + (4 * (j & 3) + (j >> 2)) * (kABoxRows * kBK * kPK), &tmA, 0,
+                      w.m0 + j * kABoxRows, kbs, full_bar(s));
+        tma_load_3d_hint(sB, &tmB, 0, brow0, kbs, full_bar(s), pol_w);
+        if (second) tma_load_3d_hint(sB + kBHalfBytes, &tmB, 0, brow1, kbs, full_bar(s), pol_w);
+        for (int k = 0; k < nv; ++k) {
+          const int kb = kbs + k;
+          bulk_copy_g2s(sS + k * kSlotAScale,
+                        static_cast<const uint8_t*>(p.a_scale) +
+                            ((size_t)kb * p.R_cap + w.m0) * (a_ue ? 1 : 4),
+                        a_scale_bytes, full_bar(s));
+          const int i0 = sr0 * KB + kb;
+          tma_load_1d(sS + kSlotW + k * kSlotWStride, &tmS, i0 - i0 % w_per16, full_bar(s));
+          if (has_sr1) {
+            const int i1 = sr1 * KB + kb;
+            tma_load_1d(sS + kSlotW + k * kSlotWStride + 128, &tmS, i1 - i1 % w_per16, full_bar(s));
+          }
         }
-        ++it;
+        ++sc;
       }
     }
-    prod_issued = it;
+    prod_issued = sc;
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA
-    int it = 0, c = 0;
+    int sc = 0, c = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-      for (int k = 0; k < kb_per_split; ++k) {
-        const int s = it % kStages;
-        const uint32_t ph = (it / kStages) & 1;
-        if (!mbar_wait(full_bar(s), ph, abort_flag, status)) {
+      const Item w = decode_item(p, item);
+      const bool second = kFC1 || (w.nb * kBN + kGroup) < p.out_cols;
+      const int kb_end = (w.ks + 1) * kb_per_split;
+      for (int st = 0; ok && st < nst_item; ++st) {
+        const int kbs = w.ks * kb_per_split + st * kPK;
+        const int nv = min(kPK, kb_end - kbs);
+        const int s = sc % kStages;
+        if (!mbar_wait(full_bar(s), (sc / kStages) & 1, abort_flag, status)) {
           ok = false;
           break;
         }
-        const int b = c & 1;
-        const uint32_t tph = (c >> 1) & 1;
-        if (!mbar_wait(tempty_bar(b), tph ^ 1, abort_flag, status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const uint32_t d = tmem_base + b * kBN;
         const uint32_t sA = sbase + s * kStageBytes;
-        const uint64_t adesc = make_sdesc_sw128(sA);
-        const uint64_t bdesc = make_sdesc_sw128(sA + kABytes);
+        const uint32_t sB = sA + kABytes;
+        for (int k = 0; k < nv; ++k) {
+          const int b = c & 1;
+          if (!mbar_wait(tempty_bar(b), ((c >> 1) & 1) ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t d = tmem_base + b * kBN;
+          const uint64_t adesc = make_sdesc_sw128(sA + k * (kABoxRows * kBK), kABoxRows * kBK * kPK);
+          const uint64_t g_desc = make_sdesc_sw128(sB + k * (kGroup * kBK));
+          const uint64_t u_desc = make_sdesc_sw128(sB + kBHalfBytes + k * (kGroup * kBK));
 #pragma unroll
-        for (int kk = 0; kk < kBK / 32; ++kk)
-          mma_f8(d, adesc + 2 * kk, bdesc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < kBK / 32; ++kk) {
+            mma_f8(d, adesc + 2 * kk, g_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+            if (second) mma_f8(d + kGroup, adesc + 2 * kk, u_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(tfull_bar(b));
+          ++c;
+        }
+        if (!ok) break;
         mma_commit(empty_bar(s));
-        mma_commit(tfull_bar(b));
-        ++it;
-        ++c;
-        *mma_consumed = it;
+        ++sc;
+        *mma_consumed = sc;
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -263,7 +291,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     const int wg = ew >> 2;                        // which half of the 256 columns
     const int q = warp & 3;                        // TMEM lane quarter this warp may access
     const int row = 32 * (lane >> 3) + 8 * q + (lane & 7);   // tile row held in lane 32q + lane
-    int c = 0;
+    int c = 0, sc = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Item w = decode_item(p, item);
@@ -275,47 +303,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       float acc[128];
 #pragma unroll
       for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-      const int kb0 = w.ks * kb_per_split;
-      for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
-        const int b = c & 1;
-        const int s = c % kStages;
-        if (!mbar_wait(tfull_bar(b), (c >> 1) & 1, abort_flag, status) ||
-            !mbar_wait(full_bar(s), (c / kStages) & 1, abort_flag, status)) {
-          ok = false;
-          break;
-        }
-        float sab0 = 0.0f, sab1 = 0.0f;
-        if (qlive) {
-          const uint8_t* slot = slots + s * kScaleSlotBytes;
-          const float sa = smem_scale_at(slot, row, a_ue);
-          const int i0 = sr0 * KB + kb, i1 = sr1 * KB + kb;
-          const float sw0 = smem_scale_at(slot + kSlotWScale0, i0 % w_per16, b_ue);
-          const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotWScale1, i1 % w_per16, b_ue) : 0.0f;
-          sab0 = __fmul_rn(sa, sw0);
-          sab1 = __fmul_rn(sa, sw1);
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));
-        tc_fence_after_sync();
-        if (qlive) {
-          const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
-          if (kFC1) {
-            promote32(t0 + wg * 64, sab0, acc);
-            promote32(t0 + wg * 64 + 32, sab0, acc + 32);
-            promote32(t0 + kGroup + wg * 64, sab1, acc + 64);
-            promote32(t0 + kGroup + wg * 64 + 32, sab1, acc + 96);
-          } else {
-            const float sab = wg == 0 ? sab0 : sab1;
-            promote32(t0 + wg * 128, sab, acc);
-            promote32(t0 + wg * 128 + 32, sab, acc + 32);
-            promote32(t0 + wg * 128 + 64, sab, acc + 64);
-            promote32(t0 + wg * 128 + 96, sab, acc + 96);
+      const int kb_end = (w.ks + 1) * kb_per_split;
+      for (int st = 0; ok && st < nst_item; ++st) {
+        const int kbs = w.ks * kb_per_split + st * kPK;
+        const int nv = min(kPK, kb_end - kbs);
+        const int s = sc % kStages;
+        const uint8_t* slot = slots + s * kScaleSlotBytes;
+        for (int k = 0; k < nv; ++k) {
+          const int b = c & 1;
+          if (!mbar_wait(tfull_bar(b), (c >> 1) & 1, abort_flag, status) ||
+              (k == 0 && !mbar_wait(full_bar(s), (sc / kStages) & 1, abort_flag, status))) {
+            ok = false;
+            break;
           }
+          const int kb = kbs + k;
+          float sab0 = 0.0f, sab1 = 0.0f;
+          if (qlive) {
+            const float sa = smem_scale_at(slot + k * kSlotAScale, row, a_ue);
+            const int i0 = sr0 * KB + kb, i1 = sr1 * KB + kb;
+            const float sw0 = smem_scale_at(slot + kSlotW + k * kSlotWStride, i0 % w_per16, b_ue);
+            const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotW + k * kSlotWStride + 128,
+                                                      i1 % w_per16, b_ue)
+                                      : 0.0f;
+            sab0 = __fmul_rn(sa, sw0);
+            sab1 = __fmul_rn(sa, sw1);
+          }
+          tc_fence_after_sync();
+          if (qlive) {
+            const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
+            if (kFC1) {
+              promote32(t0 + wg * 64, sab0, acc);
+              promote32(t0 + wg * 64 + 32, sab0, acc + 32);
+              promote32(t0 + kGroup + wg * 64, sab1, acc + 64);
+              promote32(t0 + kGroup + wg * 64 + 32, sab1, acc + 96);
+            } else {
+              const float sab = wg == 0 ? sab0 : sab1;
+              promote32(t0 + wg * 128, sab, acc);
+              promote32(t0 + wg * 128 + 32, sab, acc + 32);
+              promote32(t0 + wg * 128 + 64, sab, acc + 64);
+              promote32(t0 + wg * 128 + 96, sab, acc + 96);
+            }
+          }
+          tc_fence_before_sync();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(tempty_bar(b));
+          ++c;
         }
-        tc_fence_before_sync();
+        if (!ok) break;
         __syncwarp();
-        if (lane == 0) mbar_arrive(tempty_bar(b));
-        ++c;
+        if (lane == 0) mbar_arrive(empty_bar(s));   // this warp has read the stage's scales
+        ++sc;
       }
       if (!ok) break;
 
@@ -401,17 +438,56 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             store_scale(p.a2_s, (size_t)w.nb * p.R_cap + w.m0 + row, s, p.act_fmt == MOE_SCALE_UE8M0);
         }
       } else {
+        // BF16 tile out through TMA stores: this warp's rows come in four 8-row groups
+        // (rows 32*g + 8*q .. +7).  The warp writes its 32 x 128 block into its own 8 KB staging
+        // buffer as 128-byte-swizzled 8 x 64 boxes and lane 0 issues the box stores without waiting
+        // for them; the buffer is reused one item later, after the stores have read it.  Groups
+        // that are only partly live (the end of an expert's rows) are written row by row instead.
         const int col0 = w.nb * kBN + wg * kGroup;
-        if (rlive && col0 < p.out_cols) {
-          uint16_t* dst = p.y + (size_t)(w.m0 + row) * p.out_cols + col0;
+        if (qlive && col0 < p.out_cols) {
+          uint8_t* buf = ystage + ew * TC::YWarpBytes;
+          const uint32_t buf_s = smem_addr(buf);
+          const int t = lane & 7;
+          const int g_mine = lane >> 3;
+          const int grow_mine = 32 * g_mine + 8 * q;
+          if (lane == 0) bulk_wait_group_read0();     // the previous item's stores have read it
+          __syncwarp();
+          if (grow_mine + 8 <= w.live) {
 #pragma unroll
-          for (int v = 0; v < 16; ++v) {
-            uint32_t wd[4];
+            for (int c = 0; c < 16; ++c) {
+              uint32_t wd[4];
 #pragma unroll
-            for (int j = 0; j < 4; ++j)
-              wd[j] = f32_to_bf16_bits(acc[v * 8 + 2 * j]) |
-                      (f32_to_bf16_bits(acc[v * 8 + 2 * j + 1]) << 16);
-            *reinterpret_cast<uint4*>(dst + v * 8) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+              for (int j = 0; j < 4; ++j)
+                wd[j] = f32_to_bf16_bits(acc[c * 8 + 2 * j]) |
+                        (f32_to_bf16_bits(acc[c * 8 + 2 * j + 1]) << 16);
+              const int box = c >> 3, cc = c & 7;
+              *reinterpret_cast<uint4*>(buf + g_mine * 2048 + box * 1024 + t * 128 + ((cc ^ t) << 4)) =
+                  make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            }
+          } else if (rlive) {
+            uint16_t* dst = p.y + (size_t)(w.m0 + row) * p.out_cols + col0;
+#pragma unroll
+            for (int v = 0; v < 16; ++v) {
+              uint32_t wd[4];
+#pragma unroll
+              for (int j = 0; j < 4; ++j)
+                wd[j] = f32_to_bf16_bits(acc[v * 8 + 2 * j]) |
+                        (f32_to_bf16_bits(acc[v * 8 + 2 * j + 1]) << 16);
+              *reinterpret_cast<uint4*>(dst + v * 8) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+            }
+          }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+#pragma unroll
+            for (int g = 0; g < 4; ++g) {
+              const int grow = 32 * g + 8 * q;
+              if (grow + 8 <= w.live) {
+                tma_store_2d(&tmY, col0, w.m0 + grow, buf_s + g * 2048);
+                tma_store_2d(&tmY, col0 + 64, w.m0 + grow, buf_s + g * 2048 + 1024);
+              }
+            }
+            bulk_commit_group();
           }
         }
       }
@@ -419,6 +495,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  if (!kFC1 && warp >= kEpiWarp0 && lane == 0) bulk_wait_group0();   // output stores complete
   __syncthreads();
   if (warp == 1 && lane == 0) {
     // every MMA this CTA issued has completed (and its barrier arrivals have landed)
@@ -426,9 +503,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     drain_wait(drain_bar, 0, status);
   }
   if (warp == 0 && lane == 0 && *abort_flag) {
-    // loads issued but never consumed are still in flight: wait for them before leaving
-    for (int it = *mma_consumed; it < prod_issued; ++it)
-      drain_wait(full_bar(it % kStages), (it / kStages) & 1, status);
+    // stages issued but never consumed are still in flight: wait for them before leaving
+    for (int st = *mma_consumed; st < prod_issued; ++st)
+      drain_wait(full_bar(st % kStages), (st / kStages) & 1, status);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -440,22 +517,23 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
 template <bool kFC1>
 static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                               const GemmParams& p, int grid, cudaStream_t s) {
+                               const CUtensorMap& tmY, const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<kFC1>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize, kGemmSmemBytes);
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         TileCfg<kFC1>::Smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_grouped_gemm<kFC1>, dim3(grid), dim3(kGemmThreads), kGemmSmemBytes, s, tmA, tmB,
-                    tmS, p);
+  return launch_pdl(k_grouped_gemm<kFC1>, dim3(grid), dim3(kGemmThreads), TileCfg<kFC1>::Smem, s, tmA,
+                    tmB, tmS, tmY, p);
 }
 
 cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                        const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_gemm<true>(tmA, tmB, tmS, p, grid, s);
+  return launch_gemm<true>(tmA, tmB, tmS, tmA, p, grid, s);   // FC1 stores no BF16 tile
 }
 
 cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                       const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_gemm<false>(tmA, tmB, tmS, p, grid, s);
+                       const CUtensorMap& tmY, const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm<false>(tmA, tmB, tmS, tmY, p, grid, s);
 }
 
 }  // namespace moe

@@ -21,27 +21,43 @@ constexpr uint64_t kWaitLimitNs = 1000000000ull;   // 1 s bound on any device-si
 constexpr float kScaleFloor = 1.0f / 229376.0f;    // 1/(448*512), rounded to fp32
 
 // ---------------------------------------------------------------- GEMM tiling
-// One CTA tile: 128 workspace rows (the MMA's M) x 256 weight rows (the MMA's N) x 128 of K per
-// stage.  FC1: the 256 weight rows are 128 gate rows and the matching 128 up rows.
+// 128-row-tile kernel: one CTA tile = 128 workspace rows (the MMA's M) x 256 weight rows (two
+// N = 128 MMAs; FC1: 128 gate rows and the matching 128 up rows) x kPK 128-wide K blocks per
+// pipeline stage.  Operands arrive through 3-D tensor maps (x = 128 bytes of K, y = rows, z = K
+// block), so every row of a stage is fetched as one kPK*128-byte contiguous run.
 constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;
-constexpr int kStages = 4;
 constexpr int kABoxRows = 8;                          // activation rows per TMA box (one swizzle atom)
-constexpr int kABytes = kBM * kBK;                    // 16 KB
-constexpr int kBBytes = kBN * kBK;                    // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
 constexpr int kGemmThreads = 320;                     // TMA warp, MMA warp, 8 epilogue warps
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiThreads = 256;
 constexpr int kTmemCols = 512;                        // two 256-column accumulators
-// Per-stage scale slot: [0, 512) the 128 activation scales of the K block (fp32 or UE8M0 bytes),
-// [512, 528) and [640, 656) the 16-byte aligned chunks holding the two weight block scales.
-constexpr int kScaleSlotBytes = 768;
-constexpr int kSlotWScale0 = 512;
-constexpr int kSlotWScale1 = 640;
-constexpr int kGemmSmemBytes = kStages * kStageBytes + kStages * kScaleSlotBytes + 1024 /*align*/ +
-                               1024 /*bars*/ + 2 * kBM * 4 /*row amax exchange*/;
+// Per-stage scale slot: [k*512, +512) the 128 activation scales of the stage's K block k (fp32 or
+// UE8M0 bytes); [1024 + k*256, +16) and [1024 + k*256 + 128, +16) the 16-byte aligned chunks
+// holding the two weight block scales of K block k.
+constexpr int kSlotAScale = 512;
+constexpr int kSlotW = 1024;
+constexpr int kSlotWStride = 256;
+constexpr int kMaxPK = 2;
+
+// Pipeline shape of the 128-row-tile kernel.  FC1 (long K, small output) streams two K blocks per
+// stage (256-byte runs per row) through two stages.  FC2 (short K, a 64 KB BF16 output tile per
+// item) uses one K block per stage, three stages, and a 64 KB staging area from which asynchronous
+// TMA stores write the output tile while the next item proceeds.
+template <bool kFC1>
+struct TileCfg {
+  static constexpr int PK = kFC1 ? 2 : 1;
+  static constexpr int Stages = kFC1 ? 2 : 3;
+  static constexpr int ABytes = kBM * kBK * PK;
+  static constexpr int BHalf = kGroup * kBK * PK;     // 128 weight rows
+  static constexpr int StageBytes = ABytes + 2 * BHalf;
+  static constexpr int SlotBytes = kSlotW + PK * kSlotWStride;
+  static constexpr int YWarpBytes = kFC1 ? 0 : 8192;  // 32 rows x 128 BF16 columns per warp
+  static constexpr int Smem = Stages * StageBytes + Stages * SlotBytes + 8 * YWarpBytes +
+                              1024 /*align*/ + 1024 /*bars*/ + 2 * kBM * 4 /*row amax*/;
+};
+static_assert(TileCfg<true>::Smem <= 232448 && TileCfg<false>::Smem <= 232448, "shared memory");
 
 struct Plan {
   moe_ws_plan ws;
@@ -67,6 +83,9 @@ struct AlignParams {
   int splitk_count_len;
   int32_t* chunk_row0;
   int32_t* num_chunks;
+  // large batches: num_ctas CTAs each align a contiguous range of pairs; per-CTA expert counts
+  int32_t* cta_hist;        // [num_ctas][E]
+  int num_ctas;
 };
 
 struct QuantParams {
@@ -143,7 +162,7 @@ cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
 cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                        const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                       const GemmParams& p, int grid, cudaStream_t s);
+                       const CUtensorMap& tmY, const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc1_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                              const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc2_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,

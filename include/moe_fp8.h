@@ -78,6 +78,7 @@ typedef enum { MOE_CLAMP_NONE = 0, MOE_CLAMP_BEFORE_SILU = 1, MOE_CLAMP_AFTER_SI
  *   tile_expert  int32[T_cap] expert of row tile i (rows [128 i, 128 i + 128)), i < num_tiles
  *   num_chunks   int32        number of live 32-row chunks (small-batch schedule)
  *   chunk_row0   int32[C_cap] first row of each live 32-row chunk (chunks never cross a segment)
+ *   align_hist   int32[align_ctas][E] per-CTA expert counts of the multi-CTA alignment
  *   a1_q         uint8[R_cap][H]       FC1 input, E4M3 codes
  *   a1_s         [H/128][R_cap]        FC1 input scales, column-major (fp32, or uint8 for UE8M0)
  *   a2_q         uint8[R_cap][I]       FC2 input, E4M3 codes
@@ -86,7 +87,7 @@ typedef enum { MOE_CLAMP_NONE = 0, MOE_CLAMP_BEFORE_SILU = 1, MOE_CLAMP_AFTER_SI
  *   splitk       fp32 partial sums and int32 tile counters of the split-K FC1 schedule */
 typedef struct {
   size_t status, num_tiles, seg_start, live_end, sorted_pair, pair_row, tile_expert;
-  size_t num_chunks, chunk_row0;
+  size_t num_chunks, chunk_row0, align_hist;
   size_t a1_q, a1_s, a2_q, a2_s, y, splitk_partial, splitk_count;
   size_t total_bytes;
   int32_t R_cap;   /* workspace rows: roundup(P_cap + min(E, P_cap) * 127, 128) */
@@ -96,6 +97,7 @@ typedef struct {
   int32_t fc1_ksplit;  /* K-split factor the forward uses for FC1 (1 = none) */
   int32_t small_batch; /* 1: the GEMMs run the small-batch schedule (32-row chunks, tokens on the
                           MMA's N side); chosen when P_cap <= 16 * E */
+  int32_t align_ctas;  /* CTAs of the alignment (1 up to 4096 pairs, then one per 1024 pairs, <= 152) */
 } moe_ws_plan;
 
 /* Workspace plan for a layer shape; returns MOE_OK or a validation status. */
@@ -112,7 +114,8 @@ size_t moe_workspace_bytes(int M_cap, int E, int H, int I, int topk, moe_scale_f
  * live_end[e]; inside a segment pairs keep ascending p.  Writes, for p < n*k, pair_row[p] (row or -1)
  * and, for live rows, sorted_pair[row] = p; tile_expert[i] for every 128-row tile i < num_tiles;
  * chunk_row0[c] for every live 32-row chunk c < num_chunks.
- * Also resets the workspace status word.  Runs as one CTA.
+ * Also resets the workspace status word.  Runs as one CTA up to 4096 pairs of capacity; above that
+ * as a per-CTA counting kernel followed by a placement kernel (same result, bit for bit).
  * topk_ids: int32 [M_cap, topk]; all outputs are sub-buffers of the workspace of the same plan. */
 moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M_cap, int topk, int E,
                      int H, int I, moe_scale_fmt act_fmt, void* workspace, size_t workspace_bytes,

@@ -53,6 +53,8 @@ def test_plan_sizes():
     assert moe.workspace_plan(1, 288, 4096, 512, 8)["fc1_ksplit"] == 4
     assert moe.workspace_plan(32, 288, 4096, 512, 8)["fc1_ksplit"] == 1
     assert moe.workspace_plan(32, 288, 4096, 512, 8)["small_batch"] == 1
+    assert moe.workspace_plan(32, 288, 4096, 512, 8)["align_ctas"] == 1
+    assert moe.workspace_plan(8192, 128, 2048, 768, 8)["align_ctas"] == 64
     assert moe.workspace_plan(4096, 32, 7168, 2048, 8)["fc1_ksplit"] == 1
     # UE8M0 scales take one byte
     p8 = moe.workspace_plan(32, 288, 4096, 512, 8, moe.SCALE_UE8M0)

@@ -39,6 +39,9 @@ ALIGN_CASES = [
     (1024, 4, 300, 257, -3, 1030),
     (5, 3, 0, 0, 0, 5),           # no tokens
     (16, 1, 64, 0, 0, 16),        # capacity but zero live tokens
+    (64, 4, 2000, 1500, -1, 66),  # multi-CTA alignment, device count below capacity
+    (16, 8, 1024, 3, 0, 16),      # multi-CTA alignment with fewer live pairs than CTAs
+    (256, 8, 4096, 4096, 0, 256), # 32768 pairs
 ]
 
 
@@ -139,6 +142,18 @@ def test_layer_small_variants(clamp_mode, limit, act_fmt):
     shape = synth.small_shape("small_v", E=12, H=512, I=384, topk=3, act_fmt=act_fmt,
                               clamp_mode=clamp_mode, limit=limit)
     _layer_check(synth.make_case("small_v", 40, 33, shape=shape))
+
+
+@pytest.mark.parametrize("clamp_mode,limit", [(0, 0.0), (1, 0.02), (2, 0.01)])
+@pytest.mark.parametrize("act_fmt,weight_fmt", [(0, 0), (1, 0), (2, 2)])
+def test_layer_tile_kernel_variants(clamp_mode, limit, act_fmt, weight_fmt):
+    """128-row-tile schedule (P_cap > 16 E): odd K-block counts (I = 384), a hidden size that
+    ends on half an output tile (H = 384), and a device token count below capacity."""
+    shape = synth.small_shape("tile_v", E=4, H=384, I=384, topk=2, act_fmt=act_fmt,
+                              weight_fmt=weight_fmt, clamp_mode=clamp_mode, limit=limit)
+    case = synth.make_case("tile_v", 96, 80, shape=shape)
+    assert moe.workspace_plan(96, 4, 384, 384, 2, act_fmt)["small_batch"] == 0
+    _layer_check(case)
 
 
 def test_layer_small_ue8m0_weights():
