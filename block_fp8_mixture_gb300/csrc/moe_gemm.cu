@@ -104,7 +104,7 @@ __device__ __forceinline__ void promote32(uint32_t taddr, float sab, float* acc)
 }
 
 template <bool kFC1>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __launch_bounds__(kTileThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmY,
                    const GemmParams p) {
@@ -180,6 +180,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 
   const int nst_item = (kb_per_split + kPK - 1) / kPK;   // pipeline stages per work item
   int prod_issued = 0;
+  if (warp < kTileEpiWarp0) {
+  // registers move from warpgroup 0 (TMA / MMA issue) to the promotion warpgroups
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kTileRegsLow));
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
     int sc = 0;
@@ -285,9 +288,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         *mma_consumed = sc;
       }
     }
-  } else if (warp >= kEpiWarp0) {
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kTileRegsHigh));
     // ---------------------------------------------------- promotion + epilogue
-    const int ew = warp - kEpiWarp0;
+    const int ew = warp - kTileEpiWarp0;
     const int wg = ew >> 2;                        // which half of the 256 columns
     const int q = warp & 3;                        // TMEM lane quarter this warp may access
     const int row = 32 * (lane >> 3) + 8 * q + (lane & 7);   // tile row held in lane 32q + lane
@@ -495,7 +500,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 
   // ---------------------------------------------------------------- teardown
-  if (!kFC1 && warp >= kEpiWarp0 && lane == 0) bulk_wait_group0();   // output stores complete
+  if (!kFC1 && warp >= kTileEpiWarp0 && lane == 0) bulk_wait_group0();   // output stores complete
   __syncthreads();
   if (warp == 1 && lane == 0) {
     // every MMA this CTA issued has completed (and its barrier arrivals have landed)
@@ -522,7 +527,7 @@ static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, c
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TileCfg<kFC1>::Smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_grouped_gemm<kFC1>, dim3(grid), dim3(kGemmThreads), TileCfg<kFC1>::Smem, s, tmA,
+  return launch_pdl(k_grouped_gemm<kFC1>, dim3(grid), dim3(kTileThreads), TileCfg<kFC1>::Smem, s, tmA,
                     tmB, tmS, tmY, p);
 }
 

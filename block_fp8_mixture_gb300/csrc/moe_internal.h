@@ -29,8 +29,17 @@ constexpr int kBM = 128;
 constexpr int kBN = 256;
 constexpr int kBK = 128;
 constexpr int kABoxRows = 8;                          // activation rows per TMA box (one swizzle atom)
-constexpr int kGemmThreads = 320;                     // TMA warp, MMA warp, 8 epilogue warps
+constexpr int kGemmThreads = 320;                     // small kernel: TMA, MMA, 8 epilogue warps
 constexpr int kEpiWarp0 = 2;
+// 128-row-tile kernel: warpgroup 0 = TMA warp, MMA warp, two idle warps (56 registers each after
+// setmaxnreg); warpgroups 1-2 = the 8 promotion/epilogue warps (224 registers each).
+constexpr int kTileThreads = 384;
+constexpr int kTileEpiWarp0 = 4;
+constexpr int kTileRegsLow = 56;
+constexpr int kTileRegsHigh = 224;
+static_assert(128 * kTileRegsLow + 256 * kTileRegsHigh <= kTileThreads * 168,
+              "register split must fit the launch allocation");
+static_assert(32 * (kTileRegsLow + 2 * kTileRegsHigh) <= 16384, "register split per sub-partition");
 constexpr int kEpiThreads = 256;
 constexpr int kTmemCols = 512;                        // two 256-column accumulators
 // Per-stage scale slot: [k*512, +512) the 128 activation scales of the stage's K block k (fp32 or
