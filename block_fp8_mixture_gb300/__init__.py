@@ -20,6 +20,8 @@ SCALE_UE8M0 = 2
 CLAMP_NONE = 0
 CLAMP_BEFORE_SILU = 1
 CLAMP_AFTER_SILU = 2
+NUMERICS_DIVIDE = 0
+NUMERICS_RECIPROCAL = 1
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = 1
@@ -57,7 +59,7 @@ class FwdArgs(ctypes.Structure):
         ("w2", ctypes.c_void_p), ("s2", ctypes.c_void_p), ("out", ctypes.c_void_p),
         ("M_cap", ctypes.c_int), ("E", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
         ("topk", ctypes.c_int), ("weight_scale_fmt", ctypes.c_int), ("act_scale_fmt", ctypes.c_int),
-        ("clamp_mode", ctypes.c_int), ("clamp_limit", ctypes.c_float),
+        ("clamp_mode", ctypes.c_int), ("clamp_limit", ctypes.c_float), ("numerics", ctypes.c_int),
     ]
 
 
@@ -68,7 +70,7 @@ SIGNATURES = {
     "moe_workspace_plan": (_I, [_I, _I, _I, _I, _I, _I, _P(WsPlan)]),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
     "moe_align": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
-    "moe_quant_act": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
+    "moe_quant_act": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
     "moe_fc1_swiglu_quant": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
     "moe_fc2": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
     "moe_topk_reduce": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
@@ -170,12 +172,12 @@ def workspace_views(ws, M_cap: int, E: int, H: int, I: int, topk: int, act_fmt: 
 
 def make_args(x, topk_ids, topk_weights, w13, s13, w2, s2, out, *, E, H, I, topk, M_cap=None,
               d_num_tokens=None, weight_fmt=SCALE_FP32, act_fmt=SCALE_FP32,
-              clamp_mode=CLAMP_NONE, clamp_limit=0.0) -> FwdArgs:
+              clamp_mode=CLAMP_NONE, clamp_limit=0.0, numerics=NUMERICS_DIVIDE) -> FwdArgs:
     if M_cap is None:
         M_cap = x.shape[0] if x is not None else topk_ids.shape[0]
     return FwdArgs(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(d_num_tokens), _ptr(w13),
                    _ptr(s13), _ptr(w2), _ptr(s2), _ptr(out), M_cap, E, H, I, topk, weight_fmt,
-                   act_fmt, clamp_mode, float(clamp_limit))
+                   act_fmt, clamp_mode, float(clamp_limit), numerics)
 
 
 def align(topk_ids, E: int, H: int, I: int, workspace, *, d_num_tokens=None,
@@ -186,10 +188,11 @@ def align(topk_ids, E: int, H: int, I: int, workspace, *, d_num_tokens=None,
 
 
 def quant_act(x, topk: int, E: int, I: int, workspace, *, d_num_tokens=None,
-              act_fmt: int = SCALE_FP32, stream=None):
+              act_fmt: int = SCALE_FP32, numerics: int = NUMERICS_DIVIDE, stream=None):
     M_cap, H = x.shape
     _check(load_library().moe_quant_act(_ptr(x), _ptr(d_num_tokens), M_cap, E, H, I, topk, act_fmt,
-                                        _ptr(workspace), workspace.numel(), _stream(stream)),
+                                        numerics, _ptr(workspace), workspace.numel(),
+                                        _stream(stream)),
            "moe_quant_act")
 
 
@@ -237,7 +240,8 @@ class MoELayer:
     """
 
     def __init__(self, w13, s13, w2, s2, *, weight_fmt=SCALE_FP32, act_fmt=SCALE_FP32,
-                 clamp_mode=CLAMP_NONE, clamp_limit=0.0, max_tokens: int, topk: int):
+                 clamp_mode=CLAMP_NONE, clamp_limit=0.0, max_tokens: int, topk: int,
+                 numerics=NUMERICS_DIVIDE):
         self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
         self.E, two_i, self.H = w13.shape
         self.I = two_i // 2
@@ -245,6 +249,7 @@ class MoELayer:
         self.M_cap = max_tokens
         self.weight_fmt, self.act_fmt = weight_fmt, act_fmt
         self.clamp_mode, self.clamp_limit = clamp_mode, clamp_limit
+        self.numerics = numerics
         self.workspace = alloc_workspace(max_tokens, self.E, self.H, self.I, topk, act_fmt,
                                          device=w13.device)
 
@@ -253,7 +258,7 @@ class MoELayer:
                          E=self.E, H=self.H, I=self.I, topk=self.topk, M_cap=x.shape[0],
                          d_num_tokens=d_num_tokens, weight_fmt=self.weight_fmt,
                          act_fmt=self.act_fmt, clamp_mode=self.clamp_mode,
-                         clamp_limit=self.clamp_limit)
+                         clamp_limit=self.clamp_limit, numerics=self.numerics)
 
     def __call__(self, x, topk_ids, topk_weights, out=None, d_num_tokens=None, stream=None):
         import torch

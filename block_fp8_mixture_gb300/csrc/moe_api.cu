@@ -203,6 +203,8 @@ static moe_status check_args(const moe_fwd_args* a, const void* ws, size_t ws_by
     return MOE_ERR_INVALID_ARG;
   if (a->clamp_mode != MOE_CLAMP_NONE && !(a->clamp_limit >= 0.0f && a->clamp_limit < 3.4e38f))
     return MOE_ERR_INVALID_ARG;
+  if (a->numerics < MOE_NUMERICS_DIVIDE || a->numerics > MOE_NUMERICS_RECIPROCAL)
+    return MOE_ERR_INVALID_ARG;
   moe_status st = make_plan(a->M_cap, a->E, a->H, a->I, a->topk, a->act_scale_fmt, pl);
   if (st != MOE_OK) return st;
   st = check_ws(*pl, ws, ws_bytes);
@@ -257,8 +259,8 @@ static moe_status run_align(const int32_t* ids, const int32_t* d_n, const Plan& 
   return launch_align(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-static moe_status run_quant(const void* x, const int32_t* d_n, const Plan& pl, void* ws,
-                            cudaStream_t s) {
+static moe_status run_quant(const void* x, const int32_t* d_n, const Plan& pl, int numerics,
+                            void* ws, cudaStream_t s) {
   if (pl.M_cap == 0) return MOE_OK;
   QuantParams p;
   p.x = static_cast<const uint16_t*>(x);
@@ -269,6 +271,7 @@ static moe_status run_quant(const void* x, const int32_t* d_n, const Plan& pl, v
   p.topk = pl.topk;
   p.R_cap = pl.ws.R_cap;
   p.fmt = pl.act_fmt;
+  p.numerics = numerics;
   p.a_q = at<uint8_t>(ws, pl.ws.a1_q);
   p.a_s = at<void>(ws, pl.ws.a1_s);
   return launch_quant(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -313,6 +316,7 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.a2_s = at<void>(ws, pl.ws.a2_s);
   p.clamp_mode = a->clamp_mode;
   p.clamp_limit = a->clamp_limit;
+  p.numerics = a->numerics;
   p.splitk_partial = at<float>(ws, pl.ws.splitk_partial);
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
   const bool small = pl.ws.small_batch != 0;
@@ -403,8 +407,8 @@ moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M
 }
 
 moe_status moe_quant_act(const void* x_bf16, const int32_t* d_num_tokens, int M_cap, int E, int H,
-                         int I, int topk, moe_scale_fmt act_fmt, void* workspace,
-                         size_t workspace_bytes, moe_stream_t stream) {
+                         int I, int topk, moe_scale_fmt act_fmt, moe_numerics numerics,
+                         void* workspace, size_t workspace_bytes, moe_stream_t stream) {
   Plan pl;
   moe_status st = make_plan(M_cap, E, H, I, topk, act_fmt, &pl);
   if (st != MOE_OK) return st;
@@ -412,7 +416,8 @@ moe_status moe_quant_act(const void* x_bf16, const int32_t* d_num_tokens, int M_
   if (st != MOE_OK) return st;
   if (M_cap > 0 && (x_bf16 == nullptr || !aligned(x_bf16, 16))) return MOE_ERR_INVALID_ARG;
   if (d_num_tokens != nullptr && !aligned(d_num_tokens, 4)) return MOE_ERR_INVALID_ARG;
-  return run_quant(x_bf16, d_num_tokens, pl, workspace, (cudaStream_t)stream);
+  if (numerics < MOE_NUMERICS_DIVIDE || numerics > MOE_NUMERICS_RECIPROCAL) return MOE_ERR_INVALID_ARG;
+  return run_quant(x_bf16, d_num_tokens, pl, numerics, workspace, (cudaStream_t)stream);
 }
 
 moe_status moe_fc1_swiglu_quant(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
@@ -447,7 +452,8 @@ moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size
   if (pl.M_cap == 0) return MOE_OK;
   const cudaStream_t s = (cudaStream_t)stream;
   if ((st = run_align(args->topk_ids, args->d_num_tokens, pl, workspace, s)) != MOE_OK) return st;
-  if ((st = run_quant(args->x, args->d_num_tokens, pl, workspace, s)) != MOE_OK) return st;
+  if ((st = run_quant(args->x, args->d_num_tokens, pl, args->numerics, workspace, s)) != MOE_OK)
+    return st;
   if ((st = run_fc1(args, pl, workspace, s)) != MOE_OK) return st;
   if ((st = run_fc2(args, pl, workspace, s)) != MOE_OK) return st;
   return run_reduce(args, pl, workspace, s);

@@ -315,6 +315,24 @@ __device__ __forceinline__ float group_scale(float amax, int fmt) {
   return s;
 }
 
+// 1x128 quantization of one value set: scale and per-element multiplier-or-divisor handling for the
+// two numerics.  Returns the scale to store; with RECIPROCAL numerics and fp32 scales *inv holds the
+// multiplier RN(448/amax) (capped at 448*512), otherwise *inv = 0 and callers divide by the scale.
+__device__ __forceinline__ float group_scale_numerics(float amax, int fmt, int numerics, float* inv) {
+  if (numerics == MOE_NUMERICS_RECIPROCAL && fmt == MOE_SCALE_FP32) {
+    const float m = fminf(__fdiv_rn(448.0f, amax), 448.0f * 512.0f);
+    *inv = m;
+    return __frcp_rn(m);
+  }
+  *inv = 0.0f;
+  return group_scale(amax, fmt);
+}
+
+// RN(v / s), or RN(v * inv) when inv != 0.
+__device__ __forceinline__ float quant_div(float v, float s, float inv) {
+  return inv != 0.0f ? __fmul_rn(v, inv) : __fdiv_rn(v, s);
+}
+
 // Scale value from a stored scale (fp32 word, or a UE8M0 byte 2^(b-127)).
 __device__ __forceinline__ float load_scale(const void* base, size_t idx, int is_ue8m0) {
   if (is_ue8m0) {

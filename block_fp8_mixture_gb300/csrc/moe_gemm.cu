@@ -415,8 +415,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         if (rlive) {
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
-            const float h = swiglu(bf16_round(acc[i]), bf16_round(acc[64 + i]), p.clamp_mode,
-                                   p.clamp_limit);
+            float h = swiglu(bf16_round(acc[i]), bf16_round(acc[64 + i]), p.clamp_mode,
+                             p.clamp_limit);
+            if (p.numerics == MOE_NUMERICS_RECIPROCAL) h = bf16_round(h);
             acc[i] = h;
             amax = fmaxf(amax, fabsf(h));
           }
@@ -426,7 +427,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         amax = fmaxf(red[row], red[kBM + row]);
         named_barrier_sync(1, kEpiThreads);
         if (rlive) {
-          const float s = group_scale(amax, p.act_fmt);
+          float inv;
+          const float s = group_scale_numerics(amax, p.act_fmt, p.numerics, &inv);
           uint8_t* dst = p.a2_q + (size_t)(w.m0 + row) * I + w.nb * kGroup + wg * 64;
 #pragma unroll
           for (int v = 0; v < 4; ++v) {
@@ -434,8 +436,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
               const float* h = acc + v * 16 + j * 4;
-              wd[j] = cvt_e4m3x2(__fdiv_rn(h[0], s), __fdiv_rn(h[1], s)) |
-                      (cvt_e4m3x2(__fdiv_rn(h[2], s), __fdiv_rn(h[3], s)) << 16);
+              wd[j] = cvt_e4m3x2(quant_div(h[0], s, inv), quant_div(h[1], s, inv)) |
+                      (cvt_e4m3x2(quant_div(h[2], s, inv), quant_div(h[3], s, inv)) << 16);
             }
             *reinterpret_cast<uint4*>(dst + v * 16) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
           }

@@ -366,8 +366,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll
         for (int c = 0; c < 16; ++c) {
           if (c < ntok) {
-            const float h = s_swiglu(bf16_round(acc0[c]), bf16_round(acc1[c]), p.clamp_mode,
-                                     p.clamp_limit);
+            float h = s_swiglu(bf16_round(acc0[c]), bf16_round(acc1[c]), p.clamp_mode,
+                               p.clamp_limit);
+            if (p.numerics == MOE_NUMERICS_RECIPROCAL) h = bf16_round(h);
             acc0[c] = h;
             float m = fabsf(h);
 #pragma unroll
@@ -380,10 +381,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
         for (int c = 0; c < 16; ++c) {
           if (c < ntok) {
             const float amax = fmaxf(fmaxf(r[c], r[16 + c]), fmaxf(r[32 + c], r[48 + c]));
-            const float s = group_scale(amax, p.act_fmt);
+            float inv;
+            const float s = group_scale_numerics(amax, p.act_fmt, p.numerics, &inv);
             const int row = w.row0 + half * 16 + c;
             p.a2_q[(size_t)row * I + w.nb * kGroup + j] =
-                (uint8_t)(cvt_e4m3x2(__fdiv_rn(acc0[c], s), 0.0f) & 0xFF);
+                (uint8_t)(cvt_e4m3x2(quant_div(acc0[c], s, inv), 0.0f) & 0xFF);
             if (j == 0)
               store_scale(p.a2_s, (size_t)w.nb * p.R_cap + row, s, p.act_fmt == MOE_SCALE_UE8M0);
           }

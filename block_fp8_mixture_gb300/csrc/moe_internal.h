@@ -103,6 +103,7 @@ struct QuantParams {
   const int32_t* pair_row;
   int M_cap, H, topk, R_cap;
   int fmt;
+  int numerics;
   uint8_t* a_q;
   void* a_s;
 };
@@ -127,6 +128,7 @@ struct GemmParams {
   int act_fmt;
   int clamp_mode;
   float clamp_limit;
+  int numerics;
   float* splitk_partial;    // [ksplit][P_cap][2I] fp32
   int32_t* splitk_count;    // [T_cap * n_blocks]
   const int32_t* sorted_pair;

@@ -42,11 +42,12 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant_act(QuantParams p) {
   for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
 #pragma unroll
   for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, d));
-  const float s = group_scale(amax, p.fmt);
-  uint32_t q0 = cvt_e4m3x2(__fdiv_rn(v[0], s), __fdiv_rn(v[1], s)) |
-                (cvt_e4m3x2(__fdiv_rn(v[2], s), __fdiv_rn(v[3], s)) << 16);
-  uint32_t q1 = cvt_e4m3x2(__fdiv_rn(v[4], s), __fdiv_rn(v[5], s)) |
-                (cvt_e4m3x2(__fdiv_rn(v[6], s), __fdiv_rn(v[7], s)) << 16);
+  float inv;
+  const float s = group_scale_numerics(amax, p.fmt, p.numerics, &inv);
+  uint32_t q0 = cvt_e4m3x2(quant_div(v[0], s, inv), quant_div(v[1], s, inv)) |
+                (cvt_e4m3x2(quant_div(v[2], s, inv), quant_div(v[3], s, inv)) << 16);
+  uint32_t q1 = cvt_e4m3x2(quant_div(v[4], s, inv), quant_div(v[5], s, inv)) |
+                (cvt_e4m3x2(quant_div(v[6], s, inv), quant_div(v[7], s, inv)) << 16);
   const int is_ue8m0 = p.fmt == MOE_SCALE_UE8M0;
   for (int j = 0; j < p.topk; ++j) {
     const int row = p.pair_row[t * p.topk + j];

@@ -67,6 +67,15 @@ typedef enum { MOE_SCALE_FP32 = 0, MOE_SCALE_FP32_POW2 = 1, MOE_SCALE_UE8M0 = 2 
  * AFTER_SILU:  min(SiLU(gate), L) * clamp(up, -L, L). */
 typedef enum { MOE_CLAMP_NONE = 0, MOE_CLAMP_BEFORE_SILU = 1, MOE_CLAMP_AFTER_SILU = 2 } moe_clamp_mode;
 
+/* Quantizer / epilogue numerics.
+ * DIVIDE (default; vLLM "per-layer activation scale format + fused SiLU+quant", Details):
+ *   codes = RNE_satfinite(x / s), s = max(RN(amax/448), RN(1/(448*512))); SwiGLU output in fp32.
+ * RECIPROCAL (TensorRT-LLM "Triton FP8-activation MoE for decode-sized batches on Hopper",
+ *   rounding-fix commit: the fused op's rounding): with fp32 scales, inv = min(RN(448/amax), 448*512),
+ *   codes = RNE_satfinite(RN(x * inv)), stored scale s = RN(1/inv); the SwiGLU output is rounded to
+ *   BF16 before its quantization.  Power-of-two scale formats quantize the same way in both modes. */
+typedef enum { MOE_NUMERICS_DIVIDE = 0, MOE_NUMERICS_RECIPROCAL = 1 } moe_numerics;
+
 /* Byte offsets of the workspace sub-buffers (all 256-byte aligned) and derived sizes.
  * Layout of each sub-buffer:
  *   status       int32        device status word (0 = ok, else a moe_status)
@@ -127,8 +136,8 @@ moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M
  * codes go to a1_q[row][g*128 ...] and the scale to a1_s[g][row] for every row = pair_row[t*k+j] >= 0.
  * x: bf16 [M_cap, H].  Requires moe_align on the same workspace first (same stream). */
 moe_status moe_quant_act(const void* x_bf16, const int32_t* d_num_tokens, int M_cap, int E, int H,
-                         int I, int topk, moe_scale_fmt act_fmt, void* workspace,
-                         size_t workspace_bytes, moe_stream_t stream);
+                         int I, int topk, moe_scale_fmt act_fmt, moe_numerics numerics,
+                         void* workspace, size_t workspace_bytes, moe_stream_t stream);
 
 /* Problem statement of one layer call. */
 typedef struct {
@@ -146,6 +155,7 @@ typedef struct {
   moe_scale_fmt act_scale_fmt;    /* FP32, FP32_POW2 or UE8M0 */
   moe_clamp_mode clamp_mode;
   float clamp_limit;              /* L >= 0 when clamp_mode != NONE */
+  moe_numerics numerics;          /* quantizer / epilogue numerics (DIVIDE by default) */
 } moe_fwd_args;
 
 /* FC1 grouped GEMM over live 128-row tiles with the SwiGLU + 1x128 requantization epilogue

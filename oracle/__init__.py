@@ -28,6 +28,8 @@ from .moe_ref import (  # noqa: F401
     CLAMP_BEFORE_SILU,
     CLAMP_NONE,
     GROUP,
+    NUMERICS_DIVIDE,
+    NUMERICS_RECIPROCAL,
     SCALE_FLOOR,
     SCALE_FP32,
     SCALE_FP32_POW2,

@@ -61,6 +61,11 @@ CLAMP_NONE = 0
 CLAMP_BEFORE_SILU = 1
 CLAMP_AFTER_SILU = 2
 
+# quantizer / epilogue numerics
+NUMERICS_DIVIDE = 0      # vLLM fused SiLU+mul+quant: x / scale, fp32 SwiGLU output
+NUMERICS_RECIPROCAL = 1  # TensorRT-LLM fused op: x * RN(448/amax), reciprocal stored as the scale,
+                         # SwiGLU output rounded to BF16 before its quantization
+
 GROUP = 128      # 1x128 activation quantization group and 128x128 weight block
 ALIGN = 128      # expert segment alignment (= GEMM tile height)
 F32 = np.float32
@@ -134,17 +139,31 @@ def group_scale(amax, fmt):
     return s
 
 
-def quant_1x128(v, fmt):
+def quant_1x128(v, fmt, numerics=NUMERICS_DIVIDE):
     """Per-1x128-group FP8 E4M3 quantization along the last axis.
 
     v: fp32 [..., K] with K % 128 == 0.
     Returns (codes uint8 [..., K], scales fp32 [..., K/128]); for UE8M0 the
     scale bytes are f32_exponent_field(scales).
+
+    NUMERICS_DIVIDE (vLLM per-layer scale page, Details): s = max(RN(amax/448),
+    RN(1/229376)), codes = q8(RN(v / s)).
+    NUMERICS_RECIPROCAL with fp32 scales (TensorRT-LLM page, rounding-fix
+    commit: multiply by 448/amax, both correctly rounded, store the reciprocal):
+    inv = min(RN(448/amax), 448*512), codes = q8(RN(v * inv)), s = RN(1/inv).
+    The cap keeps the same scale floor (and handles amax = 0).  Power-of-two
+    formats quantize identically in both modes (v/s = v*(1/s) exactly).
     """
     v = np.asarray(v, F32)
     k = v.shape[-1]
     g = v.reshape(v.shape[:-1] + (k // GROUP, GROUP))
     amax = np.abs(g).max(axis=-1)
+    if numerics == NUMERICS_RECIPROCAL and fmt == SCALE_FP32:
+        with np.errstate(divide="ignore"):
+            inv = np.minimum(F32(448.0) / amax, F32(448.0 * 512.0)).astype(F32)
+        q = e4m3_encode((g * inv[..., None]).astype(F32))
+        s = (F32(1.0) / inv).astype(F32)
+        return q.reshape(v.shape), s
     s = group_scale(amax, fmt)
     q = e4m3_encode(g / s[..., None])           # fp32 IEEE division
     return q.reshape(v.shape), s
@@ -217,17 +236,20 @@ def swiglu(gate, up, clamp_mode=CLAMP_NONE, limit=0.0):
 
 # ------------------------------------------------------------ expert FFN
 def expert_rows(x_rows, w13_q, s13, w2_q, s2, act_fmt, weight_fmt,
-                clamp_mode=CLAMP_NONE, limit=0.0, intermediates=False):
+                clamp_mode=CLAMP_NONE, limit=0.0, intermediates=False,
+                numerics=NUMERICS_DIVIDE):
     """One expert applied to a set of BF16 token rows (fp32 holding BF16 values).
 
     Returns Y (fp32 holding BF16 values, [R, H]); with intermediates=True also
     a dict with A1 codes/scales, G1, A2 codes/scales.
     """
     inter = w13_q.shape[0] // 2
-    a1_q, a1_s = quant_1x128(x_rows, act_fmt)
+    a1_q, a1_s = quant_1x128(x_rows, act_fmt, numerics)
     g1 = bf16_round(block_gemm(a1_q, a1_s, w13_q, weight_scales_f32(s13, weight_fmt)))
     h = swiglu(g1[:, :inter], g1[:, inter:], clamp_mode, limit)
-    a2_q, a2_s = quant_1x128(h, act_fmt)
+    if numerics == NUMERICS_RECIPROCAL:
+        h = bf16_round(h)
+    a2_q, a2_s = quant_1x128(h, act_fmt, numerics)
     y = bf16_round(block_gemm(a2_q, a2_s, w2_q, weight_scales_f32(s2, weight_fmt)))
     if intermediates:
         return y, {"a1_q": a1_q, "a1_s": a1_s, "g1": g1, "h": h, "a2_q": a2_q, "a2_s": a2_s}
@@ -250,7 +272,7 @@ def topk_reduce(y_pairs, weights, present):
 def moe_forward(x, topk_ids, topk_weights, w13_q, s13, w2_q, s2, *,
                 act_fmt=SCALE_FP32, weight_fmt=SCALE_FP32,
                 clamp_mode=CLAMP_NONE, limit=0.0, tokens=None,
-                return_pairs=False):
+                return_pairs=False, numerics=NUMERICS_DIVIDE):
     """Full layer forward for the selected tokens (default: all rows of x).
 
     x: fp32 [M, H] holding BF16 values; topk_ids int [M, k]; topk_weights fp32
@@ -273,7 +295,8 @@ def moe_forward(x, topk_ids, topk_weights, w13_q, s13, w2_q, s2, *,
     for e in np.unique(ids[present]):
         sel_t, sel_j = np.nonzero(ids == e)
         y, inter = expert_rows(x[tokens[sel_t]], w13_q[e], s13[e], w2_q[e], s2[e],
-                               act_fmt, weight_fmt, clamp_mode, limit, intermediates=True)
+                               act_fmt, weight_fmt, clamp_mode, limit, intermediates=True,
+                               numerics=numerics)
         y_pairs[sel_t, sel_j] = y
         if return_pairs:
             for i, (ti, j) in enumerate(zip(sel_t, sel_j)):

@@ -49,6 +49,7 @@ class LayerShape:
     routing: str = "softmax"       # softmax | zipf | softmax_empty4
     outliers: float = 0.0          # fraction of x elements multiplied by 10
     cfg_id: int = 0
+    numerics: int = 0              # 0: divide by the scale; 1: multiply by RN(448/amax)
 
 
 SHAPES = {

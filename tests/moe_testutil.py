@@ -49,7 +49,7 @@ def run_forward(case: synth.LayerCase, dev=None, *, poison=True, use_device_n=Tr
                          out, E=sh.E, H=sh.H, I=sh.I, topk=sh.topk, M_cap=case.M_cap,
                          d_num_tokens=dev["n"] if use_device_n else None,
                          weight_fmt=sh.weight_fmt, act_fmt=sh.act_fmt, clamp_mode=sh.clamp_mode,
-                         clamp_limit=sh.limit)
+                         clamp_limit=sh.limit, numerics=sh.numerics)
     moe.forward(args, ws, stream)
     views = moe.workspace_views(ws, case.M_cap, sh.E, sh.H, sh.I, sh.topk, sh.act_fmt)
     return out, ws, views
@@ -62,7 +62,7 @@ def oracle_forward(case: synth.LayerCase, tokens=None, return_pairs=False):
     return oracle.moe_forward(case.x, case.topk_ids, case.topk_weights, w.w13, w.s13, w.w2, w.s2,
                               act_fmt=sh.act_fmt, weight_fmt=sh.weight_fmt,
                               clamp_mode=sh.clamp_mode, limit=sh.limit, tokens=tokens,
-                              return_pairs=return_pairs)
+                              return_pairs=return_pairs, numerics=sh.numerics)
 
 
 def bf16_tensor_to_f32(t) -> np.ndarray:

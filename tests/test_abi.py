@@ -105,7 +105,8 @@ def test_forward_validates_before_launch(lib):
     # zero-capacity layer: valid, nothing to do
     assert fwd(ctypes.byref(_args(M_cap=0)), ws, lib.moe_workspace_bytes(0, 8, 512, 256, 2, 0), None) == moe.MOE_OK
     assert lib.moe_align(None, None, 16, 2, 8, 512, 256, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
-    assert lib.moe_quant_act(None, None, 16, 8, 512, 256, 2, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_quant_act(None, None, 16, 8, 512, 256, 2, 0, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
+    assert fwd(ctypes.byref(_args(numerics=2)), ws, need, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

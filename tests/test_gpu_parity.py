@@ -73,10 +73,11 @@ def test_align_bit_exact(E, topk, M_cap, n, lo, hi):
 
 
 # ------------------------------------------------------------------ quant
-@pytest.mark.parametrize("fmt", [moe.SCALE_FP32, moe.SCALE_FP32_POW2, moe.SCALE_UE8M0])
+@pytest.mark.parametrize("fmt,numerics", [(moe.SCALE_FP32, 0), (moe.SCALE_FP32_POW2, 0),
+                                          (moe.SCALE_UE8M0, 0), (moe.SCALE_FP32, 1)])
 @pytest.mark.parametrize("H,M_cap,n,outliers", [(512, 16, 16, 0.0), (7168, 64, 40, 0.0),
                                                 (2048, 300, 300, 0.01), (4096, 3, 1, 0.0)])
-def test_quant_bit_exact(fmt, H, M_cap, n, outliers):
+def test_quant_bit_exact(fmt, numerics, H, M_cap, n, outliers):
     E, topk, I = 16, 4, 256
     rng = np.random.default_rng(H + M_cap + fmt)
     x = rng.standard_normal((M_cap, H)).astype(np.float32)
@@ -92,13 +93,13 @@ def test_quant_bit_exact(fmt, H, M_cap, n, outliers):
     ws.fill_(0xFF)
     d_n = torch.tensor([n], dtype=torch.int32, device="cuda")
     moe.align(torch.from_numpy(ids).cuda(), E, H, I, ws, d_num_tokens=d_n, act_fmt=fmt)
-    moe.quant_act(xt.cuda(), topk, E, I, ws, d_num_tokens=d_n, act_fmt=fmt)
+    moe.quant_act(xt.cuda(), topk, E, I, ws, d_num_tokens=d_n, act_fmt=fmt, numerics=numerics)
     torch.cuda.synchronize()
     v = moe.workspace_views(ws, M_cap, E, H, I, topk, fmt)
     pair_row = v["pair_row"].cpu().numpy()
     a1q = v["a1_q"].cpu().numpy()
     a1s = v["a1_s"].cpu().numpy()
-    q_ref, s_ref = oracle.quant_1x128(x_f[:n], fmt)
+    q_ref, s_ref = oracle.quant_1x128(x_f[:n], fmt, numerics)
     for t in range(n):
         for j in range(topk):
             row = pair_row[t * topk + j]
@@ -154,6 +155,24 @@ def test_layer_tile_kernel_variants(clamp_mode, limit, act_fmt, weight_fmt):
     case = synth.make_case("tile_v", 96, 80, shape=shape)
     assert moe.workspace_plan(96, 4, 384, 384, 2, act_fmt)["small_batch"] == 0
     _layer_check(case)
+
+
+@pytest.mark.parametrize("shape_kw,M,n", [
+    (dict(E=12, H=512, I=384, topk=3), 40, 33),                     # small-batch schedule
+    (dict(E=4, H=384, I=384, topk=2), 96, 80),                      # 128-row-tile schedule
+    (dict(E=4, H=384, I=384, topk=2, clamp_mode=1, limit=0.02), 96, 96),
+])
+def test_layer_reciprocal_numerics(shape_kw, M, n):
+    """TensorRT-LLM fused-op numerics: multiply by RN(448/amax), BF16-rounded SwiGLU output."""
+    shape = synth.small_shape("recip", numerics=1, **shape_kw)
+    _layer_check(synth.make_case("recip", M, n, shape=shape))
+
+
+def test_layer_decode_reciprocal_numerics():
+    base = synth.SHAPES["decode"]
+    shape = synth.LayerShape("decode_r", base.E, base.H, base.I, base.topk,
+                             clamp_mode=base.clamp_mode, limit=base.limit, cfg_id=2, numerics=1)
+    _layer_check(synth.make_case("decode_r", 4, shape=shape))
 
 
 def test_layer_small_ue8m0_weights():

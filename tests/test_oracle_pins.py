@@ -501,3 +501,52 @@ def test_planted_mistakes_are_caught(monkeypatch, small_case):
     bad = np.linalg.norm(_fwd(c) - ref) / np.linalg.norm(ref)
     monkeypatch.setattr(moe_ref, "weight_scales_f32", orig_ws)
     assert good < 0.1 <= bad
+
+
+# ------------------------------------------- reciprocal (TensorRT-LLM) numerics
+def test_reciprocal_quant_closed_form():
+    R = oracle.NUMERICS_RECIPROCAL
+    amax = np.array([448.0, 896.0, 3.0, 0.0, 1e-9], F32)
+    v = np.zeros((5, 128), F32)
+    v[:, 0] = amax
+    q, s = oracle.quant_1x128(v, oracle.SCALE_FP32, R)
+    inv3 = F32(448.0) / F32(3.0)
+    assert s[0, 0] == 1.0 and s[1, 0] == 2.0
+    assert s[2, 0] == F32(1.0) / inv3
+    assert s[3, 0] == oracle.SCALE_FLOOR and s[4, 0] == F32(1.0) / F32(229376.0)
+    assert np.all(q[3] == 0)
+    # the group maximum maps to the nearest E4M3 of amax * RN(448/amax) (448 or a neighbour)
+    assert fm.E4M3_VALUES[q[2, 0]] == fm.E4M3_VALUES[fm.e4m3_encode(np.array([F32(3.0) * inv3]))[0]]
+
+
+def test_reciprocal_quant_differs_from_division_on_bf16_inputs():
+    """The two quantizers disagree on some BF16 inputs that sit on E4M3 midpoints (the reason the
+    TensorRT-LLM page gives for matching the fused op), and each is its own nearest rounding."""
+    rng = np.random.default_rng(21)
+    v = fm.bf16_round((rng.standard_normal((4000, 128)) * 3).astype(F32))
+    qd, sd = oracle.quant_1x128(v, oracle.SCALE_FP32, oracle.NUMERICS_DIVIDE)
+    qr, sr = oracle.quant_1x128(v, oracle.SCALE_FP32, oracle.NUMERICS_RECIPROCAL)
+    assert np.count_nonzero(qd != qr) > 0
+    inv = F32(448.0) / np.abs(v).max(axis=1)
+    assert np.array_equal(qr, fm.e4m3_encode((v * inv[:, None]).astype(F32)))
+    assert np.array_equal(sr[:, 0], (F32(1.0) / inv).astype(F32))
+    # power-of-two formats: the two numerics coincide
+    for fmt in (oracle.SCALE_FP32_POW2, oracle.SCALE_UE8M0):
+        a = oracle.quant_1x128(v[:50], fmt, oracle.NUMERICS_DIVIDE)
+        b = oracle.quant_1x128(v[:50], fmt, oracle.NUMERICS_RECIPROCAL)
+        assert np.array_equal(a[0], b[0]) and np.array_equal(a[1], b[1])
+
+
+def test_reciprocal_numerics_rounds_swiglu_output_to_bf16(small_case):
+    c = small_case
+    w = c.weights
+    e = int(c.topk_ids[0, 0])
+    _, inter = oracle.expert_rows(c.x[:3], w.w13[e], w.s13[e], w.w2[e], w.s2[e], 0, 0,
+                                  intermediates=True, numerics=oracle.NUMERICS_RECIPROCAL)
+    assert np.array_equal(inter["h"], fm.bf16_round(inter["h"]))
+    _, inter0 = oracle.expert_rows(c.x[:3], w.w13[e], w.s13[e], w.w2[e], w.s2[e], 0, 0,
+                                   intermediates=True)
+    assert not np.array_equal(inter0["h"], fm.bf16_round(inter0["h"]))
+    ref = dense_reference(c)
+    out = _fwd(c, numerics=oracle.NUMERICS_RECIPROCAL)
+    assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 0.1
