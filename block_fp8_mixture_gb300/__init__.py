@@ -60,6 +60,7 @@ class FwdArgs(ctypes.Structure):
         ("M_cap", ctypes.c_int), ("E", ctypes.c_int), ("H", ctypes.c_int), ("I", ctypes.c_int),
         ("topk", ctypes.c_int), ("weight_scale_fmt", ctypes.c_int), ("act_scale_fmt", ctypes.c_int),
         ("clamp_mode", ctypes.c_int), ("clamp_limit", ctypes.c_float), ("numerics", ctypes.c_int),
+        ("expert_offset", ctypes.c_int), ("out_fp32", ctypes.c_int),
     ]
 
 
@@ -69,7 +70,7 @@ _VP, _SZ, _I, _P = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTE
 SIGNATURES = {
     "moe_workspace_plan": (_I, [_I, _I, _I, _I, _I, _I, _P(WsPlan)]),
     "moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I, _I]),
-    "moe_align": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
+    "moe_align": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
     "moe_quant_act": (_I, [_VP, _VP, _I, _I, _I, _I, _I, _I, _I, _VP, _SZ, _VP]),
     "moe_fc1_swiglu_quant": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
     "moe_fc2": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
@@ -172,19 +173,31 @@ def workspace_views(ws, M_cap: int, E: int, H: int, I: int, topk: int, act_fmt: 
 
 def make_args(x, topk_ids, topk_weights, w13, s13, w2, s2, out, *, E, H, I, topk, M_cap=None,
               d_num_tokens=None, weight_fmt=SCALE_FP32, act_fmt=SCALE_FP32,
-              clamp_mode=CLAMP_NONE, clamp_limit=0.0, numerics=NUMERICS_DIVIDE) -> FwdArgs:
+              clamp_mode=CLAMP_NONE, clamp_limit=0.0, numerics=NUMERICS_DIVIDE, expert_offset=0,
+              out_fp32=False) -> FwdArgs:
     if M_cap is None:
         M_cap = x.shape[0] if x is not None else topk_ids.shape[0]
     return FwdArgs(_ptr(x), _ptr(topk_ids), _ptr(topk_weights), _ptr(d_num_tokens), _ptr(w13),
                    _ptr(s13), _ptr(w2), _ptr(s2), _ptr(out), M_cap, E, H, I, topk, weight_fmt,
-                   act_fmt, clamp_mode, float(clamp_limit), numerics)
+                   act_fmt, clamp_mode, float(clamp_limit), numerics, expert_offset,
+                   1 if out_fp32 else 0)
 
 
 def align(topk_ids, E: int, H: int, I: int, workspace, *, d_num_tokens=None,
-          act_fmt: int = SCALE_FP32, stream=None):
+          act_fmt: int = SCALE_FP32, expert_offset: int = 0, stream=None):
     M_cap, topk = topk_ids.shape
-    _check(load_library().moe_align(_ptr(topk_ids), _ptr(d_num_tokens), M_cap, topk, E, H, I, act_fmt,
-                                    _ptr(workspace), workspace.numel(), _stream(stream)), "moe_align")
+    _check(load_library().moe_align(_ptr(topk_ids), _ptr(d_num_tokens), M_cap, topk, E, expert_offset,
+                                    H, I, act_fmt, _ptr(workspace), workspace.numel(),
+                                    _stream(stream)), "moe_align")
+
+
+def expert_slice(num_experts: int, world: int, rank: int):
+    """(first expert, expert count) of `rank` when `world` ranks split the experts into contiguous,
+    near-equal slices (the first num_experts % world ranks hold one more)."""
+    base, extra = divmod(num_experts, world)
+    count = base + (1 if rank < extra else 0)
+    first = rank * base + min(rank, extra)
+    return first, count
 
 
 def quant_act(x, topk: int, E: int, I: int, workspace, *, d_num_tokens=None,
@@ -241,7 +254,7 @@ class MoELayer:
 
     def __init__(self, w13, s13, w2, s2, *, weight_fmt=SCALE_FP32, act_fmt=SCALE_FP32,
                  clamp_mode=CLAMP_NONE, clamp_limit=0.0, max_tokens: int, topk: int,
-                 numerics=NUMERICS_DIVIDE):
+                 numerics=NUMERICS_DIVIDE, expert_offset: int = 0, out_fp32: bool = False):
         self.w13, self.s13, self.w2, self.s2 = w13, s13, w2, s2
         self.E, two_i, self.H = w13.shape
         self.I = two_i // 2
@@ -250,6 +263,7 @@ class MoELayer:
         self.weight_fmt, self.act_fmt = weight_fmt, act_fmt
         self.clamp_mode, self.clamp_limit = clamp_mode, clamp_limit
         self.numerics = numerics
+        self.expert_offset, self.out_fp32 = expert_offset, out_fp32
         self.workspace = alloc_workspace(max_tokens, self.E, self.H, self.I, topk, act_fmt,
                                          device=w13.device)
 
@@ -258,13 +272,15 @@ class MoELayer:
                          E=self.E, H=self.H, I=self.I, topk=self.topk, M_cap=x.shape[0],
                          d_num_tokens=d_num_tokens, weight_fmt=self.weight_fmt,
                          act_fmt=self.act_fmt, clamp_mode=self.clamp_mode,
-                         clamp_limit=self.clamp_limit, numerics=self.numerics)
+                         clamp_limit=self.clamp_limit, numerics=self.numerics,
+                         expert_offset=self.expert_offset, out_fp32=self.out_fp32)
 
     def __call__(self, x, topk_ids, topk_weights, out=None, d_num_tokens=None, stream=None):
         import torch
         if x.shape[0] > self.M_cap:
             raise ValueError(f"{x.shape[0]} tokens exceed the layer's capacity {self.M_cap}")
         if out is None:
-            out = torch.empty_like(x)
+            out = torch.empty(x.shape, dtype=torch.float32 if self.out_fp32 else x.dtype,
+                              device=x.device)
         forward(self.args(x, topk_ids, topk_weights, out, d_num_tokens), self.workspace, stream)
         return out

@@ -5,7 +5,8 @@
 // TensorRT-LLM "Triton FP8-activation MoE for decode-sized batches on Hopper", description: one
 // program aligns the routed pairs.)
 //
-// A stable counting sort of the valid pairs p = t*k + j (t < n) by expert.  The pairs are cut into
+// A stable counting sort of the valid pairs p = t*k + j (t < n) by expert (ids rebased by the
+// expert-parallel offset; ids outside [0, E) are dropped).  The pairs are cut into
 // G contiguous ranges, one per CTA (G = 1 for small batches).  Inside a CTA the 32 warps each own a
 // contiguous sub-range:
 //   pass 1  each warp counts its sub-range per expert (warp-private histogram row, no atomics:
@@ -79,7 +80,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align_count(AlignParams p)
   const int begin = min((int)blockIdx.x * per, num_pairs);
   const int end = min(begin + per, num_pairs);
   for (int i = begin + threadIdx.x; i < end; i += kAlignThreads) {
-    const int id = p.topk_ids[i];
+    const int id = p.topk_ids[i] - p.expert_offset;
     if (id >= 0 && id < E) atomicAdd(&hist[id], 1);
   }
   __syncthreads();
@@ -120,7 +121,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
     const int pi = b0 + lane;
     int e = -1;
     if (pi < end) {
-      const int id = p.topk_ids[pi];
+      const int id = p.topk_ids[pi] - p.expert_offset;
       if (id >= 0 && id < E) e = id;
     }
     const uint32_t same = __match_any_sync(0xFFFFFFFFu, e);
@@ -185,7 +186,7 @@ __global__ void __launch_bounds__(kAlignThreads, 1) k_align(AlignParams p) {
     const int pi = b0 + lane;
     int e = -1;
     if (pi < end) {
-      const int id = p.topk_ids[pi];
+      const int id = p.topk_ids[pi] - p.expert_offset;
       if (id >= 0 && id < E) e = id;
     }
     const uint32_t same = __match_any_sync(0xFFFFFFFFu, e);

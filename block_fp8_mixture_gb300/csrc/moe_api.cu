@@ -235,14 +235,15 @@ static T* at(void* ws, size_t off) {
 }
 
 // ------------------------------------------------------------- steps
-static moe_status run_align(const int32_t* ids, const int32_t* d_n, const Plan& pl, void* ws,
-                            cudaStream_t s) {
+static moe_status run_align(const int32_t* ids, const int32_t* d_n, int expert_offset, const Plan& pl,
+                            void* ws, cudaStream_t s) {
   AlignParams p;
   p.topk_ids = ids;
   p.d_num_tokens = d_n;
   p.M_cap = pl.M_cap;
   p.topk = pl.topk;
   p.E = pl.E;
+  p.expert_offset = expert_offset;
   p.seg_start = at<int32_t>(ws, pl.ws.seg_start);
   p.live_end = at<int32_t>(ws, pl.ws.live_end);
   p.sorted_pair = at<int32_t>(ws, pl.ws.sorted_pair);
@@ -369,7 +370,8 @@ static moe_status run_reduce(const moe_fwd_args* a, const Plan& pl, void* ws, cu
   p.M_cap = pl.M_cap;
   p.H = pl.H;
   p.topk = pl.topk;
-  p.out = static_cast<uint16_t*>(a->out);
+  p.out = a->out;
+  p.out_fp32 = a->out_fp32 ? 1 : 0;
   return launch_reduce(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -394,8 +396,8 @@ size_t moe_workspace_bytes(int M_cap, int E, int H, int I, int topk, moe_scale_f
 }
 
 moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M_cap, int topk, int E,
-                     int H, int I, moe_scale_fmt act_fmt, void* workspace, size_t workspace_bytes,
-                     moe_stream_t stream) {
+                     int expert_offset, int H, int I, moe_scale_fmt act_fmt, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream) {
   Plan pl;
   moe_status st = make_plan(M_cap, E, H, I, topk, act_fmt, &pl);
   if (st != MOE_OK) return st;
@@ -403,7 +405,7 @@ moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M
   if (st != MOE_OK) return st;
   if (M_cap > 0 && (topk_ids == nullptr || !aligned(topk_ids, 4))) return MOE_ERR_INVALID_ARG;
   if (d_num_tokens != nullptr && !aligned(d_num_tokens, 4)) return MOE_ERR_INVALID_ARG;
-  return run_align(topk_ids, d_num_tokens, pl, workspace, (cudaStream_t)stream);
+  return run_align(topk_ids, d_num_tokens, expert_offset, pl, workspace, (cudaStream_t)stream);
 }
 
 moe_status moe_quant_act(const void* x_bf16, const int32_t* d_num_tokens, int M_cap, int E, int H,
@@ -451,7 +453,9 @@ moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size
   if (st != MOE_OK) return st;
   if (pl.M_cap == 0) return MOE_OK;
   const cudaStream_t s = (cudaStream_t)stream;
-  if ((st = run_align(args->topk_ids, args->d_num_tokens, pl, workspace, s)) != MOE_OK) return st;
+  if ((st = run_align(args->topk_ids, args->d_num_tokens, args->expert_offset, pl, workspace, s)) !=
+      MOE_OK)
+    return st;
   if ((st = run_quant(args->x, args->d_num_tokens, pl, args->numerics, workspace, s)) != MOE_OK)
     return st;
   if ((st = run_fc1(args, pl, workspace, s)) != MOE_OK) return st;

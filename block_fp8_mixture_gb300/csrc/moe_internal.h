@@ -81,6 +81,7 @@ struct AlignParams {
   const int32_t* topk_ids;
   const int32_t* d_num_tokens;
   int M_cap, topk, E;
+  int expert_offset;
   int32_t* seg_start;
   int32_t* live_end;
   int32_t* sorted_pair;
@@ -147,7 +148,8 @@ struct ReduceParams {
   const float* topk_weights;
   const int32_t* d_num_tokens;
   int M_cap, H, topk;
-  uint16_t* out;
+  void* out;                // bf16, or fp32 when out_fp32
+  int out_fp32;
 };
 
 // Launch with programmatic stream serialization: the kernel may start while the previous kernel of

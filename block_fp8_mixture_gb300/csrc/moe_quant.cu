@@ -67,7 +67,8 @@ cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
 // ----------------------------------------------------------------- reduce
 // (TensorRT-LLM page, rounding-fix commit: the routing weights scale the BF16 expert outputs in
 // fp32 in the top-k sum, not the FC2 accumulators.)
-// out[t, c] = bf16( sum_j RN(RN(w[t,j] * y[row_j, c]) ) ) over pairs j with a row, j ascending.
+// out[t, c] = bf16( sum_j RN(RN(w[t,j] * y[row_j, c]) ) ) over pairs j with a row, j ascending
+// (the fp32 sum itself when out_fp32: an expert-parallel rank's partial output).
 // Each thread produces 8 consecutive columns (16-byte loads of y and a 16-byte store).
 constexpr int kReduceThreads = 128;
 
@@ -95,11 +96,18 @@ __global__ void __launch_bounds__(kReduceThreads) k_topk_reduce(ReduceParams p) 
       acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, bf16_bits_to_f32(u[i] >> 16)));
     }
   }
+  if (p.out_fp32) {
+    float* o = static_cast<float*>(p.out) + t * p.H + c0;
+    *reinterpret_cast<float4*>(o) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(o + 4) = make_float4(acc[4], acc[5], acc[6], acc[7]);
+    return;
+  }
   uint32_t o[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i)
     o[i] = f32_to_bf16_bits(acc[2 * i]) | (f32_to_bf16_bits(acc[2 * i + 1]) << 16);
-  *reinterpret_cast<uint4*>(p.out + t * p.H + c0) = make_uint4(o[0], o[1], o[2], o[3]);
+  *reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + t * p.H + c0) =
+      make_uint4(o[0], o[1], o[2], o[3]);
 }
 
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t s) {

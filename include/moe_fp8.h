@@ -123,12 +123,14 @@ size_t moe_workspace_bytes(int M_cap, int E, int H, int I, int topk, moe_scale_f
  * live_end[e]; inside a segment pairs keep ascending p.  Writes, for p < n*k, pair_row[p] (row or -1)
  * and, for live rows, sorted_pair[row] = p; tile_expert[i] for every 128-row tile i < num_tiles;
  * chunk_row0[c] for every live 32-row chunk c < num_chunks.
+ * expert_offset: the call holds experts [expert_offset, expert_offset + E) of a larger set (an
+ * expert-parallel slice; 0 for a whole layer): ids are rebased by the offset, the others dropped.
  * Also resets the workspace status word.  Runs as one CTA up to 4096 pairs of capacity; above that
  * as a per-CTA counting kernel followed by a placement kernel (same result, bit for bit).
  * topk_ids: int32 [M_cap, topk]; all outputs are sub-buffers of the workspace of the same plan. */
 moe_status moe_align(const int32_t* topk_ids, const int32_t* d_num_tokens, int M_cap, int topk, int E,
-                     int H, int I, moe_scale_fmt act_fmt, void* workspace, size_t workspace_bytes,
-                     moe_stream_t stream);
+                     int expert_offset, int H, int I, moe_scale_fmt act_fmt, void* workspace,
+                     size_t workspace_bytes, moe_stream_t stream);
 
 /* Per-1x128 activation quantization scattered to the aligned workspace (vLLM per-layer scale page,
  * Details: scale = max(amax/448, 1/(448*512)), codes = RNE_satfinite(x/scale) with IEEE division;
@@ -156,6 +158,13 @@ typedef struct {
   moe_clamp_mode clamp_mode;
   float clamp_limit;              /* L >= 0 when clamp_mode != NONE */
   moe_numerics numerics;          /* quantizer / epilogue numerics (DIVIDE by default) */
+  /* Expert-parallel slice (TensorRT-LLM page, review of expert-parallel masking: drop ids outside
+   * [0, E) instead of computing them with zero weight): the weights hold experts
+   * [expert_offset, expert_offset + E) of a larger set; other ids are dropped.  0 for a whole layer. */
+  int expert_offset;
+  /* 0: out is BF16.  1: out is fp32 [M_cap, H], the unrounded top-k sum, so that expert-parallel
+   * ranks can add their partial outputs and round to BF16 once. */
+  int out_fp32;
 } moe_fwd_args;
 
 /* FC1 grouped GEMM over live 128-row tiles with the SwiGLU + 1x128 requantization epilogue

@@ -73,7 +73,7 @@ SCALE_FLOOR = F32(1.0) / F32(448.0 * 512.0)   # RN32(1/229376)
 
 
 # ---------------------------------------------------------------- alignment
-def align(topk_ids, n_tokens, num_experts, align_to=ALIGN, chunk_rows=32):
+def align(topk_ids, n_tokens, num_experts, align_to=ALIGN, chunk_rows=32, expert_offset=0):
     """Routing alignment into per-expert prefix-sum endpoints.
 
     Pairs p = t*topk + j for t < n_tokens; a pair is valid when its id is in
@@ -90,8 +90,10 @@ def align(topk_ids, n_tokens, num_experts, align_to=ALIGN, chunk_rows=32):
     (pair of each live row, -1 on padding rows), tile_expert[num_tiles],
     num_tiles, and the small-batch work list: chunk_row0 = the first row of each
     chunk_rows-row piece of every expert's live rows (experts ascending), num_chunks.
+    With expert_offset, this call holds experts [offset, offset + num_experts) of a larger set:
+    ids are rebased by the offset and the others dropped (expert-parallel slice).
     """
-    topk_ids = np.asarray(topk_ids, np.int64)
+    topk_ids = np.asarray(topk_ids, np.int64) - expert_offset   # local expert ids
     topk = topk_ids.shape[1]
     num_pairs = n_tokens * topk
     ids = topk_ids.reshape(-1)[:num_pairs]
@@ -257,22 +259,22 @@ def expert_rows(x_rows, w13_q, s13, w2_q, s2, act_fmt, weight_fmt,
 
 
 # ---------------------------------------------------------------- reduce
-def topk_reduce(y_pairs, weights, present):
+def topk_reduce(y_pairs, weights, present, out_fp32=False):
     """out = RNbf16(sum_j RN32(w_j * y_j)) accumulated in fp32, j ascending,
-    over the pairs that are present (valid ids)."""
+    over the pairs that are present (valid ids); out_fp32 returns the fp32 sum unrounded."""
     topk = weights.shape[-1]
     acc = np.zeros(y_pairs.shape[:1] + y_pairs.shape[2:], F32)
     for j in range(topk):
         term = (np.asarray(weights[:, j], F32)[:, None] * y_pairs[:, j]).astype(F32)
         acc = np.where(present[:, j][:, None], (acc + term).astype(F32), acc)
-    return bf16_round(acc)
+    return acc if out_fp32 else bf16_round(acc)
 
 
 # ------------------------------------------------------------------ layer
 def moe_forward(x, topk_ids, topk_weights, w13_q, s13, w2_q, s2, *,
                 act_fmt=SCALE_FP32, weight_fmt=SCALE_FP32,
                 clamp_mode=CLAMP_NONE, limit=0.0, tokens=None,
-                return_pairs=False, numerics=NUMERICS_DIVIDE):
+                return_pairs=False, numerics=NUMERICS_DIVIDE, expert_offset=0, out_fp32=False):
     """Full layer forward for the selected tokens (default: all rows of x).
 
     x: fp32 [M, H] holding BF16 values; topk_ids int [M, k]; topk_weights fp32
@@ -280,6 +282,9 @@ def moe_forward(x, topk_ids, topk_weights, w13_q, s13, w2_q, s2, *,
     bytes); w2_q uint8 [E, H, I]; s2 [E, H/128, I/128].
     Returns out (fp32 holding BF16 values) [len(tokens), H]; with
     return_pairs=True also the per-pair dict {(t, j): (Y row, intermediates)}.
+    expert_offset: the weights hold experts [offset, offset + E) of a larger set (an
+    expert-parallel slice); other ids are dropped.  out_fp32: return the fp32 sum (the
+    partial output a rank contributes before the cross-rank sum) instead of BF16.
     """
     x = np.asarray(x, F32)
     num_experts = w13_q.shape[0]
@@ -288,7 +293,7 @@ def moe_forward(x, topk_ids, topk_weights, w13_q, s13, w2_q, s2, *,
         tokens = np.arange(x.shape[0])
     tokens = np.asarray(tokens, np.int64)
     topk = topk_ids.shape[1]
-    ids = np.asarray(topk_ids, np.int64)[tokens]
+    ids = np.asarray(topk_ids, np.int64)[tokens] - expert_offset
     present = (ids >= 0) & (ids < num_experts)
     y_pairs = np.zeros((tokens.size, topk, hidden), F32)
     pairs = {}
@@ -302,7 +307,7 @@ def moe_forward(x, topk_ids, topk_weights, w13_q, s13, w2_q, s2, *,
             for i, (ti, j) in enumerate(zip(sel_t, sel_j)):
                 pairs[(int(tokens[ti]), int(j))] = (
                     y[i], {k: v[i] for k, v in inter.items()})
-    out = topk_reduce(y_pairs, np.asarray(topk_weights, F32)[tokens], present)
+    out = topk_reduce(y_pairs, np.asarray(topk_weights, F32)[tokens], present, out_fp32)
     if return_pairs:
         return out, pairs
     return out

@@ -104,7 +104,7 @@ def test_forward_validates_before_launch(lib):
     assert fwd(ctypes.byref(_args(weight_scale_fmt=0, s13=258)), ws, need, None) == moe.MOE_ERR_INVALID_ARG
     # zero-capacity layer: valid, nothing to do
     assert fwd(ctypes.byref(_args(M_cap=0)), ws, lib.moe_workspace_bytes(0, 8, 512, 256, 2, 0), None) == moe.MOE_OK
-    assert lib.moe_align(None, None, 16, 2, 8, 512, 256, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
+    assert lib.moe_align(None, None, 16, 2, 8, 0, 512, 256, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_act(None, None, 16, 8, 512, 256, 2, 0, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
     assert fwd(ctypes.byref(_args(numerics=2)), ws, need, None) == moe.MOE_ERR_INVALID_ARG
 
@@ -114,3 +114,12 @@ def test_missing_library_fails_loudly(monkeypatch, tmp_path):
     monkeypatch.setattr(moe, "LIBPATH", str(tmp_path / "nope.so"))
     with pytest.raises(RuntimeError, match="no fallback"):
         moe.load_library()
+
+
+def test_expert_slices_partition_the_experts():
+    for E in (1, 7, 16, 288):
+        for world in (1, 2, 3, 8):
+            spans = [moe.expert_slice(E, world, r) for r in range(world)]
+            covered = [e for first, count in spans for e in range(first, first + count)]
+            assert covered == list(range(E))
+            assert max(c for _, c in spans) - min(c for _, c in spans) <= 1

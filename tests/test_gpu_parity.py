@@ -270,3 +270,37 @@ def test_graph_replay_changing_routing():
         ref = oracle_forward(case)
         assert_layer_close(gpu[:n], ref, f"replay n={n}")
         assert bool((out[n:].view(torch.int16) == -1).all())
+
+
+@pytest.mark.parametrize("world", [2, 3])
+def test_expert_parallel_virtual_ranks(world):
+    """Expert-parallel slices run one after another on one GPU ("virtual ranks"): each rank's fp32
+    partial matches the oracle's partial, rows t >= n stay untouched, and the rank-ordered fp32 sum
+    rounded once to BF16 matches the whole layer."""
+    E, H, I, k, M, n = 16, 512, 256, 4, 64, 50
+    shape = synth.small_shape("ep_gpu", E=E, H=H, I=I, topk=k)
+    case = synth.make_case("ep_gpu", M, n, shape=shape)
+    dev = device_case(case)
+    w = case.weights
+    total = torch.zeros((M, H), dtype=torch.float32, device="cuda")
+    whole = oracle_forward(case)
+    for r in range(world):
+        first, cnt = moe.expert_slice(E, world, r)
+        sl = slice(first, first + cnt)
+        ws = moe.alloc_workspace(M, cnt, H, I, k)
+        out = torch.full((M, H), float("nan"), dtype=torch.float32, device="cuda")
+        args = moe.make_args(dev["x"], dev["ids"], dev["w"], dev["w13"][sl], dev["s13"][sl],
+                             dev["w2"][sl], dev["s2"][sl], out, E=cnt, H=H, I=I, topk=k, M_cap=M,
+                             d_num_tokens=dev["n"], expert_offset=first, out_fp32=True)
+        moe.forward(args, ws)
+        torch.cuda.synchronize()
+        assert moe.last_device_status(ws) == moe.MOE_OK
+        part = out.cpu().numpy()
+        ref = oracle.moe_forward(case.x, case.topk_ids, case.topk_weights, w.w13[sl], w.s13[sl],
+                                 w.w2[sl], w.s2[sl], expert_offset=first, out_fp32=True,
+                                 tokens=np.arange(n))
+        assert np.all(np.isnan(part[n:]))
+        assert np.abs(part[:n] - ref).max() <= 1e-2 * float(np.abs(whole).max())
+        total += out.nan_to_num(0.0)
+    got = oracle.bf16_round(total.cpu().numpy()[:n])
+    assert_layer_close(got, whole, f"expert parallel x{world}")

@@ -550,3 +550,43 @@ def test_reciprocal_numerics_rounds_swiglu_output_to_bf16(small_case):
     ref = dense_reference(c)
     out = _fwd(c, numerics=oracle.NUMERICS_RECIPROCAL)
     assert np.linalg.norm(out - ref) / np.linalg.norm(ref) < 0.1
+
+
+# --------------------------------------------------------- expert-parallel slice
+def test_expert_slices_sum_to_the_whole_layer(small_case):
+    """Ranks holding contiguous expert slices produce fp32 partials whose sum, rounded once to
+    BF16, is the whole layer up to the order of the fp32 additions."""
+    c = small_case
+    w = c.weights
+    full32 = _fwd(c, out_fp32=True)
+    E = c.shape.E
+    for world in (2, 3):
+        total = np.zeros_like(full32)
+        terms = np.zeros_like(full32)
+        for r in range(world):
+            base, extra = divmod(E, world)
+            cnt = base + (1 if r < extra else 0)
+            first = r * base + min(r, extra)
+            part = oracle.moe_forward(c.x, c.topk_ids, c.topk_weights, w.w13[first:first + cnt],
+                                      w.s13[first:first + cnt], w.w2[first:first + cnt],
+                                      w.s2[first:first + cnt], expert_offset=first, out_fp32=True)
+            total = (total + part).astype(F32)
+            terms += np.abs(part)
+        bound = 4 * 2.0 ** -23 * (terms + np.abs(full32))
+        assert np.all(np.abs(total - full32) <= bound + 1e-30)
+        assert np.mean(fm.bf16_round(total) == fm.bf16_round(full32)) > 0.99
+
+
+def test_expert_offset_drops_ids_outside_the_slice(small_case):
+    c = small_case
+    w = c.weights
+    first, cnt = 2, 3
+    part = oracle.moe_forward(c.x, c.topk_ids, c.topk_weights, w.w13[first:first + cnt],
+                              w.s13[first:first + cnt], w.w2[first:first + cnt],
+                              w.s2[first:first + cnt], expert_offset=first)
+    ids = c.topk_ids.copy()
+    ids[(ids < first) | (ids >= first + cnt)] = -1
+    masked = synth.LayerCase(c.shape, c.M_cap, c.n, c.x_bits, c.x, ids, c.topk_weights, c.weights)
+    assert np.array_equal(part, _fwd(masked))
+    a = oracle.align(c.topk_ids, c.n, cnt, expert_offset=first)
+    assert (a["live_end"] - a["seg_start"][:-1]).sum() == np.count_nonzero(ids >= 0)
