@@ -64,6 +64,17 @@ class FwdArgs(ctypes.Structure):
     ]
 
 
+class BatchedArgs(ctypes.Structure):
+    _fields_ = [
+        ("x", ctypes.c_void_p), ("d_counts", ctypes.c_void_p), ("w13", ctypes.c_void_p),
+        ("s13", ctypes.c_void_p), ("w2", ctypes.c_void_p), ("s2", ctypes.c_void_p),
+        ("out", ctypes.c_void_p), ("E", ctypes.c_int), ("max_m", ctypes.c_int),
+        ("H", ctypes.c_int), ("I", ctypes.c_int), ("weight_scale_fmt", ctypes.c_int),
+        ("act_scale_fmt", ctypes.c_int), ("clamp_mode", ctypes.c_int),
+        ("clamp_limit", ctypes.c_float), ("numerics", ctypes.c_int),
+    ]
+
+
 _LIB = None
 # every function the header declares, with its ctypes signature (restype, argtypes)
 _VP, _SZ, _I, _P = ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int, ctypes.POINTER
@@ -77,6 +88,8 @@ SIGNATURES = {
     "moe_topk_reduce": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
     "moe_fp8_block_forward": (_I, [_P(FwdArgs), _VP, _SZ, _VP]),
     "moe_fp8_block_forward_static": (_I, [_P(FwdArgs), _VP]),
+    "moe_batched_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "moe_fp8_batched_forward": (_I, [_P(BatchedArgs), _VP, _SZ, _VP]),
     "moe_last_device_status": (_I, [_VP, _VP]),
     "moe_status_str": (ctypes.c_char_p, [_I]),
     "moe_version": (ctypes.c_char_p, []),
@@ -239,6 +252,34 @@ def forward_static(args: FwdArgs, stream=None):
 
 
 STATIC_SCRATCH_BYTES = 32 << 20
+
+
+def batched_workspace_bytes(E: int, max_m: int, H: int, I: int, act_fmt: int = SCALE_FP32) -> int:
+    n = load_library().moe_batched_workspace_bytes(E, max_m, H, I, act_fmt)
+    if n == 0:
+        raise MoeError(MOE_ERR_UNSUPPORTED_SHAPE, "moe_batched_workspace_bytes")
+    return n
+
+
+def alloc_batched_workspace(E: int, max_m: int, H: int, I: int, act_fmt: int = SCALE_FP32,
+                            device="cuda"):
+    import torch
+    return torch.empty(batched_workspace_bytes(E, max_m, H, I, act_fmt), dtype=torch.uint8,
+                       device=device)
+
+
+def batched_forward(x, d_counts, w13, s13, w2, s2, out, workspace, *, weight_fmt=SCALE_FP32,
+                    act_fmt=SCALE_FP32, clamp_mode=CLAMP_NONE, clamp_limit=0.0,
+                    numerics=NUMERICS_DIVIDE, stream=None):
+    """The batched-expert layer (moe_fp8_batched_forward): x and out [E, max_m, H] BF16, d_counts
+    device int32 [E]; rows r >= counts[e] of out are left as they were."""
+    E, max_m, H = x.shape
+    a = BatchedArgs(_ptr(x), _ptr(d_counts), _ptr(w13), _ptr(s13), _ptr(w2), _ptr(s2), _ptr(out),
+                    E, max_m, H, w13.shape[1] // 2, weight_fmt, act_fmt, clamp_mode, clamp_limit,
+                    numerics)
+    _check(load_library().moe_fp8_batched_forward(ctypes.byref(a), _ptr(workspace),
+                                                  workspace.numel(), _stream(stream)),
+           "moe_fp8_batched_forward")
 
 
 def last_device_status(workspace, stream=None) -> int:

@@ -221,3 +221,42 @@ cudaError_t launch_align(const AlignParams& p, cudaStream_t s) {
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// Batched-expert layout (vLLM "per-layer activation scale format + fused SiLU+quant", Details:
+// batched experts with masked per-expert counts): expert e's rows already sit at
+// [e * max_m, e * max_m + counts[e]) (max_m a multiple of 128), so no sort is needed -- only the
+// live ends and the compact lists of live 128-row tiles and 32-row chunks the GEMMs walk.
+__global__ void __launch_bounds__(kAlignThreads, 1) k_batch_prep(BatchPrepParams p) {
+  __shared__ int32_t warp_sums[kAlignWarps];
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  const int tid = threadIdx.x;
+  if (tid == 0) *p.status = 0;
+  int count = 0;
+  if (tid < p.E) count = min(max(p.counts[tid], 0), p.max_m);
+  int tiles_total = 0, chunks_total = 0;
+  const int tile_base = block_exclusive_scan((count + kAlign - 1) / kAlign, warp_sums, &tiles_total);
+  const int chunk_base =
+      block_exclusive_scan((count + kChunkRows - 1) / kChunkRows, warp_sums, &chunks_total);
+  if (tid < p.E) {
+    const int r0 = tid * p.max_m;
+    p.seg_start[tid] = r0;
+    p.live_end[tid] = r0 + count;
+    for (int t = 0; t * kAlign < count; ++t) p.tile_row0[tile_base + t] = r0 + t * kAlign;
+    for (int c = 0; c * kChunkRows < count; ++c) p.chunk_row0[chunk_base + c] = r0 + c * kChunkRows;
+    for (int t = 0; t < p.max_m / kAlign; ++t) p.tile_expert[r0 / kAlign + t] = tid;
+  }
+  if (tid == 0) {
+    p.seg_start[p.E] = p.E * p.max_m;
+    *p.num_tiles = tiles_total;
+    *p.num_chunks = chunks_total;
+  }
+}
+
+cudaError_t launch_batch_prep(const BatchPrepParams& p, cudaStream_t s) {
+  return launch_pdl(k_batch_prep, dim3(1), dim3(kAlignThreads), 0, s, p);
+}
+
+}  // namespace moe

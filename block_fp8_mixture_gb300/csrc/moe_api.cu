@@ -293,7 +293,8 @@ static void fill_gemm_common(GemmParams& p, const Plan& pl, void* ws) {
   p.num_chunks = at<int32_t>(ws, pl.ws.num_chunks);
 }
 
-static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {
+static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s,
+                          const int32_t* tile_row0 = nullptr) {
   if (pl.ws.R_cap == 0) return MOE_OK;
   CUtensorMap tmA, tmB, tmS;
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
@@ -305,6 +306,7 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
     return MOE_ERR_CUDA;
   GemmParams p;
   fill_gemm_common(p, pl, ws);
+  p.tile_row0 = tile_row0;
   p.a_scale = at<void>(ws, pl.ws.a1_s);
   p.b_scale = a->s13;
   p.b_scale_ue8m0 = a->weight_scale_fmt == MOE_SCALE_UE8M0;
@@ -328,7 +330,8 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s) {
+static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s,
+                          const int32_t* tile_row0 = nullptr, void* y_target = nullptr) {
   if (pl.ws.R_cap == 0) return MOE_OK;
   CUtensorMap tmA, tmB, tmS;
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
@@ -340,6 +343,7 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
     return MOE_ERR_CUDA;
   GemmParams p;
   fill_gemm_common(p, pl, ws);
+  p.tile_row0 = tile_row0;
   p.a_scale = at<void>(ws, pl.ws.a2_s);
   p.b_scale = a->s2;
   p.b_scale_ue8m0 = a->weight_scale_fmt == MOE_SCALE_UE8M0;
@@ -348,12 +352,13 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.b_rows_per_expert = pl.H;
   p.out_cols = pl.H;
   p.ksplit = 1;
-  p.y = at<uint16_t>(ws, pl.ws.y);
+  void* y = y_target != nullptr ? y_target : at<void>(ws, pl.ws.y);
+  p.y = static_cast<uint16_t*>(y);
   const bool small = pl.ws.small_batch != 0;
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
   CUtensorMap tmY;
-  if (!small && !make_map_bf16_store(&tmY, at<void>(ws, pl.ws.y), pl.H, pl.ws.R_cap))
+  if (!small && !make_map_bf16_store(&tmY, y, pl.H, pl.ws.R_cap))
     return MOE_ERR_CUDA;
   const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
                                 : launch_fc2(tmA, tmB, tmS, tmY, p, grid, s);
@@ -373,6 +378,55 @@ static moe_status run_reduce(const moe_fwd_args* a, const Plan& pl, void* ws, cu
   p.out = a->out;
   p.out_fp32 = a->out_fp32 ? 1 : 0;
   return launch_reduce(p, s) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ------------------------------------------------- batched-expert layout
+// Expert e's rows are [e * max_m, e * max_m + counts[e]) of x [E, max_m, H] and of out; the
+// workspace holds the metadata and the FP8 intermediates of the same row space.
+static moe_status make_batched_plan(int E, int max_m, int H, int I, int act_fmt, Plan* plan,
+                                    size_t* tile_row0_off) {
+  if (E <= 0 || max_m <= 0 || H <= 0 || I <= 0) return MOE_ERR_INVALID_ARG;
+  if (act_fmt < MOE_SCALE_FP32 || act_fmt > MOE_SCALE_UE8M0) return MOE_ERR_INVALID_ARG;
+  if (max_m % kAlign || H % kGroup || I % kGroup || H > 32768 || I > 16384 || E > kMaxExperts)
+    return MOE_ERR_UNSUPPORTED_SHAPE;
+  if ((long long)E * max_m > kMaxPairs) return MOE_ERR_UNSUPPORTED_SHAPE;
+  memset(plan, 0, sizeof(*plan));
+  moe_ws_plan& w = plan->ws;
+  const long long R = (long long)E * max_m;
+  w.R_cap = (int32_t)R;
+  w.P_cap = (int32_t)R;
+  w.T_cap = (int32_t)(R / kAlign);
+  w.C_cap = (int32_t)(R / 32);
+  w.small_batch = max_m <= 256 ? 1 : 0;
+  w.fc1_ksplit = 1;
+  w.align_ctas = 1;
+  const size_t sc = act_fmt == MOE_SCALE_UE8M0 ? 1 : 4;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  w.status = take(4);
+  w.num_tiles = take(4);
+  w.seg_start = take((size_t)(E + 1) * 4);
+  w.live_end = take((size_t)E * 4);
+  w.tile_expert = take((size_t)w.T_cap * 4);
+  *tile_row0_off = take((size_t)w.T_cap * 4);
+  w.num_chunks = take(4);
+  w.chunk_row0 = take((size_t)w.C_cap * 4);
+  w.a1_q = take((size_t)R * H);
+  w.a1_s = take((size_t)(H / kGroup) * R * sc);
+  w.a2_q = take((size_t)R * I);
+  w.a2_s = take((size_t)(I / kGroup) * R * sc);
+  w.total_bytes = off;
+  plan->M_cap = max_m;
+  plan->E = E;
+  plan->H = H;
+  plan->I = I;
+  plan->topk = 1;
+  plan->act_fmt = act_fmt;
+  return MOE_OK;
 }
 
 }  // namespace moe
@@ -461,6 +515,77 @@ moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size
   if ((st = run_fc1(args, pl, workspace, s)) != MOE_OK) return st;
   if ((st = run_fc2(args, pl, workspace, s)) != MOE_OK) return st;
   return run_reduce(args, pl, workspace, s);
+}
+
+size_t moe_batched_workspace_bytes(int E, int max_m, int H, int I, moe_scale_fmt act_fmt) {
+  Plan pl;
+  size_t tr;
+  return make_batched_plan(E, max_m, H, I, act_fmt, &pl, &tr) == MOE_OK ? pl.ws.total_bytes : 0;
+}
+
+moe_status moe_fp8_batched_forward(const moe_batched_args* b, void* workspace,
+                                   size_t workspace_bytes, moe_stream_t stream) {
+  if (b == nullptr) return MOE_ERR_INVALID_ARG;
+  Plan pl;
+  size_t tile_row0_off = 0;
+  moe_status st = make_batched_plan(b->E, b->max_m, b->H, b->I, b->act_scale_fmt, &pl, &tile_row0_off);
+  if (st != MOE_OK) return st;
+  if ((st = check_ws(pl, workspace, workspace_bytes)) != MOE_OK) return st;
+  if (b->weight_scale_fmt < MOE_SCALE_FP32 || b->weight_scale_fmt > MOE_SCALE_UE8M0 ||
+      b->clamp_mode < MOE_CLAMP_NONE || b->clamp_mode > MOE_CLAMP_AFTER_SILU ||
+      b->numerics < MOE_NUMERICS_DIVIDE || b->numerics > MOE_NUMERICS_RECIPROCAL)
+    return MOE_ERR_INVALID_ARG;
+  if (b->clamp_mode != MOE_CLAMP_NONE && !(b->clamp_limit >= 0.0f && b->clamp_limit < 3.4e38f))
+    return MOE_ERR_INVALID_ARG;
+  if (b->x == nullptr || !aligned(b->x, 16) || b->out == nullptr || !aligned(b->out, 16) ||
+      b->d_counts == nullptr || !aligned(b->d_counts, 4) || b->w13 == nullptr ||
+      !aligned(b->w13, 16) || b->w2 == nullptr || !aligned(b->w2, 16) || b->s13 == nullptr ||
+      !aligned(b->s13, 16) || b->s2 == nullptr || !aligned(b->s2, 16))
+    return MOE_ERR_INVALID_ARG;
+  const cudaStream_t s = (cudaStream_t)stream;
+  int32_t* tile_row0 = at<int32_t>(workspace, tile_row0_off);
+  BatchPrepParams bp;
+  bp.counts = b->d_counts;
+  bp.E = b->E;
+  bp.max_m = b->max_m;
+  bp.seg_start = at<int32_t>(workspace, pl.ws.seg_start);
+  bp.live_end = at<int32_t>(workspace, pl.ws.live_end);
+  bp.tile_expert = at<int32_t>(workspace, pl.ws.tile_expert);
+  bp.tile_row0 = tile_row0;
+  bp.num_tiles = at<int32_t>(workspace, pl.ws.num_tiles);
+  bp.chunk_row0 = at<int32_t>(workspace, pl.ws.chunk_row0);
+  bp.num_chunks = at<int32_t>(workspace, pl.ws.num_chunks);
+  bp.status = at<int32_t>(workspace, pl.ws.status);
+  if (launch_batch_prep(bp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  QuantRowsParams qp;
+  qp.x = static_cast<const uint16_t*>(b->x);
+  qp.counts = b->d_counts;
+  qp.E = b->E;
+  qp.max_m = b->max_m;
+  qp.H = b->H;
+  qp.R_cap = pl.ws.R_cap;
+  qp.fmt = b->act_scale_fmt;
+  qp.numerics = b->numerics;
+  qp.a_q = at<uint8_t>(workspace, pl.ws.a1_q);
+  qp.a_s = at<void>(workspace, pl.ws.a1_s);
+  if (launch_quant_rows(qp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  moe_fwd_args a;
+  memset(&a, 0, sizeof(a));
+  a.w13 = b->w13;
+  a.s13 = b->s13;
+  a.w2 = b->w2;
+  a.s2 = b->s2;
+  a.E = b->E;
+  a.H = b->H;
+  a.I = b->I;
+  a.weight_scale_fmt = b->weight_scale_fmt;
+  a.act_scale_fmt = b->act_scale_fmt;
+  a.clamp_mode = b->clamp_mode;
+  a.clamp_limit = b->clamp_limit;
+  a.numerics = b->numerics;
+  const int32_t* tiles = pl.ws.small_batch ? nullptr : tile_row0;
+  if ((st = run_fc1(&a, pl, workspace, s, tiles)) != MOE_OK) return st;
+  return run_fc2(&a, pl, workspace, s, tiles, b->out);
 }
 
 moe_status moe_last_device_status(const void* workspace, moe_stream_t stream) {

@@ -46,8 +46,9 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
   const int rem = item - it.tile * per_tile;
   it.nb = rem / p.ksplit;
   it.ks = rem - it.nb * p.ksplit;
-  it.e = p.tile_expert[it.tile];
-  it.m0 = it.tile * kBM;
+  // tiles are contiguous from row 0 (routed layer) or listed (batched-expert layout)
+  it.m0 = p.tile_row0 != nullptr ? p.tile_row0[it.tile] : it.tile * kBM;
+  it.e = p.tile_expert[it.m0 / kBM];
   it.live = min(kBM, p.live_end[it.e] - it.m0);
   return it;
 }

@@ -98,6 +98,30 @@ struct AlignParams {
   int num_ctas;
 };
 
+// Batched-expert layout: expert e's rows are [e * max_m, e * max_m + counts[e]).
+struct BatchPrepParams {
+  const int32_t* counts;
+  int E, max_m;
+  int32_t* seg_start;
+  int32_t* live_end;
+  int32_t* tile_expert;
+  int32_t* tile_row0;
+  int32_t* num_tiles;
+  int32_t* chunk_row0;
+  int32_t* num_chunks;
+  int32_t* status;
+};
+
+struct QuantRowsParams {
+  const uint16_t* x;
+  const int32_t* counts;
+  int E, max_m, H, R_cap;
+  int fmt;
+  int numerics;
+  uint8_t* a_q;
+  void* a_s;
+};
+
 struct QuantParams {
   const uint16_t* x;
   const int32_t* d_num_tokens;
@@ -137,6 +161,8 @@ struct GemmParams {
   // small-batch schedule: live 32-row chunks
   const int32_t* chunk_row0;
   const int32_t* num_chunks;
+  // batched-expert layout: first row of each live 128-row tile (nullptr: tile i starts at 128 i)
+  const int32_t* tile_row0;
   // FC2 epilogue
   uint16_t* y;
   int32_t* status;
@@ -171,6 +197,8 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 cudaError_t launch_align(const AlignParams& p, cudaStream_t s);
+cudaError_t launch_batch_prep(const BatchPrepParams& p, cudaStream_t s);
+cudaError_t launch_quant_rows(const QuantRowsParams& p, cudaStream_t s);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
 cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                        const GemmParams& p, int grid, cudaStream_t s);

@@ -117,3 +117,54 @@ cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t s) {
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// Batched-expert layout: quantize rows r < counts[e] of x [E, max_m, H] in place of the scatter
+// (workspace row = e * max_m + r; same arithmetic as k_quant_act).
+__global__ void __launch_bounds__(kQuantThreads) k_quant_rows(QuantRowsParams p) {
+  const int groups_per_row = p.H / kGroup;
+  const int half = (threadIdx.x >> 4) & 1;
+  const int l16 = threadIdx.x & 15;
+  const uint32_t hmask = 0xFFFFu << (16 * half);
+  const long gid = (long)blockIdx.x * kGroupsPerBlock + (threadIdx.x >> 4);
+  const long row = gid / groups_per_row;
+  const int g = (int)(gid % groups_per_row);
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  if (row >= (long)p.E * p.max_m) return;
+  const int e = (int)(row / p.max_m);
+  const int r = (int)(row - (long)e * p.max_m);
+  if (r >= min(max(p.counts[e], 0), p.max_m)) return;   // the whole half-warp leaves together
+
+  const uint4 raw = *reinterpret_cast<const uint4*>(p.x + row * p.H + g * kGroup + l16 * 8);
+  float v[8];
+  const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = bf16_bits_to_f32(w[i] & 0xFFFFu);
+    v[2 * i + 1] = bf16_bits_to_f32(w[i] >> 16);
+  }
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+#pragma unroll
+  for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, d));
+  float inv;
+  const float s = group_scale_numerics(amax, p.fmt, p.numerics, &inv);
+  const uint32_t q0 = cvt_e4m3x2(quant_div(v[0], s, inv), quant_div(v[1], s, inv)) |
+                      (cvt_e4m3x2(quant_div(v[2], s, inv), quant_div(v[3], s, inv)) << 16);
+  const uint32_t q1 = cvt_e4m3x2(quant_div(v[4], s, inv), quant_div(v[5], s, inv)) |
+                      (cvt_e4m3x2(quant_div(v[6], s, inv), quant_div(v[7], s, inv)) << 16);
+  *reinterpret_cast<uint2*>(p.a_q + (size_t)row * p.H + g * kGroup + l16 * 8) = make_uint2(q0, q1);
+  if (l16 == 0) store_scale(p.a_s, (size_t)g * p.R_cap + row, s, p.fmt == MOE_SCALE_UE8M0);
+}
+
+cudaError_t launch_quant_rows(const QuantRowsParams& p, cudaStream_t s) {
+  const long groups = (long)p.E * p.max_m * (p.H / kGroup);
+  const long blocks = (groups + kGroupsPerBlock - 1) / kGroupsPerBlock;
+  if (blocks == 0) return cudaSuccess;
+  return launch_pdl(k_quant_rows, dim3((unsigned)blocks), dim3(kQuantThreads), 0, s, p);
+}
+
+}  // namespace moe

@@ -215,6 +215,34 @@ moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size
  *  - The device status word of these calls is not readable through moe_last_device_status. */
 moe_status moe_fp8_block_forward_static(const moe_fwd_args* args, moe_stream_t stream);
 
+/* Batched-expert layout (vLLM per-layer scale page, Details, batched experts: per-expert rows with
+ * masked counts, no host-side count reads).  x and out are [E, max_m, H] BF16; expert e's live rows
+ * are r < counts[e] (device int32 [E], clamped to [0, max_m]); rows r >= counts[e] of out are never
+ * written.  The layer runs per expert without routing: out[e, r] = FC2(SwiGLU-requant(FC1(
+ * quant(x[e, r])))) in BF16 -- the dispatch and the weighted combine happen outside (e.g. in an
+ * expert-parallel exchange).  max_m must be a multiple of 128; E * max_m <= 2^20. */
+typedef struct {
+  const void* x;               /* bf16 [E, max_m, H] */
+  const int32_t* d_counts;     /* device int32 [E] */
+  const void* w13;             /* E4M3 [E, 2I, H] */
+  const void* s13;             /* [E, 2I/128, H/128] fp32 or UE8M0 */
+  const void* w2;              /* E4M3 [E, H, I] */
+  const void* s2;              /* [E, H/128, I/128] */
+  void* out;                   /* bf16 [E, max_m, H] */
+  int E, max_m, H, I;
+  moe_scale_fmt weight_scale_fmt, act_scale_fmt;
+  moe_clamp_mode clamp_mode;
+  float clamp_limit;
+  moe_numerics numerics;
+} moe_batched_args;
+
+/* Workspace bytes of moe_fp8_batched_forward (0 if the shape is unsupported). */
+size_t moe_batched_workspace_bytes(int E, int max_m, int H, int I, moe_scale_fmt act_fmt);
+
+/* The batched-expert layer on `stream`; same numerics and status conventions as the routed forward. */
+moe_status moe_fp8_batched_forward(const moe_batched_args* args, void* workspace,
+                                   size_t workspace_bytes, moe_stream_t stream);
+
 /* Reads the workspace status word (synchronizes `stream` first).  MOE_OK or MOE_ERR_DEVICE_TIMEOUT. */
 moe_status moe_last_device_status(const void* workspace, moe_stream_t stream);
 

@@ -35,6 +35,7 @@ from .moe_ref import (  # noqa: F401
     SCALE_FP32_POW2,
     SCALE_UE8M0,
     align,
+    batched_forward,
     block_gemm,
     expert_rows,
     group_scale,

@@ -311,3 +311,29 @@ def moe_forward(x, topk_ids, topk_weights, w13_q, s13, w2_q, s2, *,
     if return_pairs:
         return out, pairs
     return out
+
+
+# ------------------------------------------------------- batched experts
+def batched_forward(x, counts, w13_q, s13, w2_q, s2, *, act_fmt=SCALE_FP32,
+                    weight_fmt=SCALE_FP32, clamp_mode=CLAMP_NONE, limit=0.0,
+                    numerics=NUMERICS_DIVIDE):
+    """Batched-expert layout (vLLM per-layer activation scale page, Details:
+    batched experts with masked per-expert counts).
+
+    x: fp32 [E, max_m, H] holding BF16 values; counts int [E].  Expert e runs
+    on its rows r < counts[e] (clamped to [0, max_m]) with no routing weight:
+    out[e, r] = expert_rows(x[e, r]).  Returns (out fp32 [E, max_m, H] holding
+    BF16 values, with NaN in the rows that are not live, and live mask [E, max_m]).
+    """
+    x = np.asarray(x, F32)
+    num_experts, max_m, hidden = x.shape
+    out = np.full((num_experts, max_m, hidden), np.nan, F32)
+    live = np.zeros((num_experts, max_m), bool)
+    for e in range(num_experts):
+        c = int(min(max(int(counts[e]), 0), max_m))
+        if c == 0:
+            continue
+        out[e, :c] = expert_rows(x[e, :c], w13_q[e], s13[e], w2_q[e], s2[e], act_fmt,
+                                 weight_fmt, clamp_mode, limit, numerics=numerics)
+        live[e, :c] = True
+    return out, live

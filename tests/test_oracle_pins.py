@@ -590,3 +590,35 @@ def test_expert_offset_drops_ids_outside_the_slice(small_case):
     assert np.array_equal(part, _fwd(masked))
     a = oracle.align(c.topk_ids, c.n, cnt, expert_offset=first)
     assert (a["live_end"] - a["seg_start"][:-1]).sum() == np.count_nonzero(ids >= 0)
+
+
+def test_batched_experts_match_the_routed_layer_and_the_dense_ffn(small_case):
+    """Batched-expert layout: expert e on its first counts[e] rows equals the routed layer with
+    one expert per token and weight 1 (out = the BF16 expert output), each live row is within FP8
+    error of the dequantized dense FFN, and rows past the count stay out of the result."""
+    c = small_case
+    w = c.weights
+    E, H = c.shape.E, c.shape.H
+    max_m = 8
+    counts = np.array([0, 8, 3, 1, 5, 8, 2, 7][:E], np.int64)
+    rng = np.random.default_rng(11)
+    xb = fm.bf16_round(rng.standard_normal((E, max_m, H)).astype(F32))
+    out, live = oracle.batched_forward(xb, counts, w.w13, w.s13, w.w2, w.s2)
+    assert live.sum() == counts.sum()
+    assert np.all(np.isnan(out[~live])) and np.all(np.isfinite(out[live]))
+    rows = xb[live]
+    ids = np.repeat(np.arange(E), counts)[:, None].astype(np.int32)
+    routed = oracle.moe_forward(rows, ids, np.ones_like(ids, dtype=F32), w.w13, w.s13, w.w2, w.s2)
+    assert np.array_equal(out[live], routed)
+    one = synth.LayerCase(c.shape, rows.shape[0], rows.shape[0], fm.bf16_bits(rows), rows, ids,
+                          np.ones(ids.shape, F32), w)
+    ref = dense_reference(one)
+    assert np.linalg.norm(out[live] - ref) / np.linalg.norm(ref) < 0.1
+    # counts are clamped to [0, max_m]; dead rows never influence live ones
+    xb2 = xb.copy()
+    xb2[~live] = 1e4
+    wild = counts.copy()
+    wild[0], wild[1] = -3, 99                 # clamp to 0 and to max_m
+    out2, live2 = oracle.batched_forward(xb2, wild, w.w13, w.s13, w.w2, w.s2)
+    assert np.array_equal(live2, live)
+    assert np.array_equal(out2[live], out[live])
