@@ -152,24 +152,61 @@ static bool make_map_bf16_store(CUtensorMap* m, void* base, uint64_t cols, uint6
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static bool make_map_u8_3d_fc1(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                               uint32_t box_outer) {
-  return make_map_u8_3d_pk(m, base, inner, outer, box_outer, TileCfg<true>::PK);
+// Activation rows [R][K] bytes of the tile kernel as a 5-D view: x = 128 bytes of a K block,
+// i = row inside an 8-row group, k = K block, a = 32-row block, b = 8-row group inside it.  One box
+// {128, 8, pk, 4, 4} at (0, 0, kb, m0/32, 0) brings the 128-row tile for pk K blocks in a single copy
+// and lays 8-row group 4a + b at shared-memory group 4b + a (each group pk x 1 KB).
+static bool make_map_act_tile(CUtensorMap* m, const void* base, uint64_t K, uint64_t R, uint32_t pk) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[5] = {(cuuint64_t)kBK, 8, K / kBK, R / 32, 4};
+  const cuuint64_t strides[4] = {K, (cuuint64_t)kBK, 32 * K, 8 * K};
+  const cuuint32_t box[5] = {(cuuint32_t)kBK, 8, pk, 4, 4};
+  const cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 5, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-static bool make_map_u8_3d_fc2(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                               uint32_t box_outer) {
-  return make_map_u8_3d_pk(m, base, inner, outer, box_outer, TileCfg<false>::PK);
+// W13 [E*2I][H] as 4-D (x, row, K block, half with a stride of I rows): one box {128, 128, pk, 2}
+// brings 128 gate rows and the matching 128 up rows.
+static bool make_map_w13_tile(CUtensorMap* m, const void* base, uint64_t H, uint64_t rows,
+                              uint64_t I, uint32_t pk) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kBK, rows, H / kBK, 2};
+  const cuuint64_t strides[3] = {H, (cuuint64_t)kBK, I * H};
+  const cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)kGroup, pk, 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Flat array of n elements (fp32 or bytes), boxes of 16 bytes: used to fetch one block scale (and
-// its 16-byte aligned neighbours) per pipeline stage.
-static bool make_map_1d(CUtensorMap* m, const void* base, bool bytes, uint64_t n) {
+// Activation scales [K/128][R] (fp32 or UE8M0 bytes) as 2-D, boxes of 128 rows x pk K blocks.
+static bool make_map_act_scales(CUtensorMap* m, const void* base, bool bytes, uint64_t R,
+                                uint64_t KB, uint32_t pk) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {R, KB};
+  const cuuint64_t strides[1] = {R * (bytes ? 1 : 4)};
+  const cuuint32_t box[2] = {(cuuint32_t)kBM, pk};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2,
+            const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Flat array of n elements (fp32 or bytes), boxes of box_bytes (16 or 32): used to fetch the block
+// scales of a pipeline stage (and their aligned neighbours).
+static bool make_map_1d(CUtensorMap* m, const void* base, bool bytes, uint64_t n,
+                        uint32_t box_bytes = 16) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t dims[1] = {n};
   const cuuint64_t strides[1] = {0};
-  const cuuint32_t box[1] = {bytes ? 16u : 4u};
+  const cuuint32_t box[1] = {bytes ? box_bytes : box_bytes / 4};
   const cuuint32_t estr[1] = {1};
   return fn(m, bytes ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 1,
             const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -296,14 +333,21 @@ static void fill_gemm_common(GemmParams& p, const Plan& pl, void* ws) {
 static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s,
                           const int32_t* tile_row0 = nullptr) {
   if (pl.ws.R_cap == 0) return MOE_OK;
-  CUtensorMap tmA, tmB, tmS;
+  CUtensorMap tmA, tmB, tmAS, tmS;
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
-  const bool small_maps = pl.ws.small_batch != 0;
-  auto mk = small_maps ? make_map_u8 : make_map_u8_3d_fc1;
-  if (!mk(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kABoxRows) ||
-      !mk(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup) ||
-      !make_map_1d(&tmS, a->s13, w_ue, (uint64_t)pl.E * (2 * pl.I / kGroup) * (pl.H / kGroup)))
-    return MOE_ERR_CUDA;
+  const bool small = pl.ws.small_batch != 0;
+  const uint64_t n_ws = (uint64_t)pl.E * (2 * pl.I / kGroup) * (pl.H / kGroup);
+  constexpr uint32_t pk = TileCfg<true>::PK;
+  const bool maps_ok =
+      small ? make_map_u8(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kABoxRows) &&
+                  make_map_u8(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup) &&
+                  make_map_1d(&tmS, a->s13, w_ue, n_ws)
+            : make_map_act_tile(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, pk) &&
+                  make_map_w13_tile(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, pl.I, pk) &&
+                  make_map_act_scales(&tmAS, at<void>(ws, pl.ws.a1_s), pl.act_fmt == MOE_SCALE_UE8M0,
+                                      pl.ws.R_cap, pl.H / kGroup, pk) &&
+                  make_map_1d(&tmS, a->s13, w_ue, n_ws, 32);
+  if (!maps_ok) return MOE_ERR_CUDA;
   GemmParams p;
   fill_gemm_common(p, pl, ws);
   p.tile_row0 = tile_row0;
@@ -322,25 +366,31 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.numerics = a->numerics;
   p.splitk_partial = at<float>(ws, pl.ws.splitk_partial);
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
-  const bool small = pl.ws.small_batch != 0;
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks * p.ksplit;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
   const cudaError_t err = small ? launch_fc1_small(tmA, tmB, tmS, p, grid, s)
-                                : launch_fc1(tmA, tmB, tmS, p, grid, s);
+                                : launch_fc1(tmA, tmB, tmAS, tmS, p, grid, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s,
                           const int32_t* tile_row0 = nullptr, void* y_target = nullptr) {
   if (pl.ws.R_cap == 0) return MOE_OK;
-  CUtensorMap tmA, tmB, tmS;
+  CUtensorMap tmA, tmB, tmAS, tmS;
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
-  const bool small_maps = pl.ws.small_batch != 0;
-  auto mk = small_maps ? make_map_u8 : make_map_u8_3d_fc2;
-  if (!mk(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kABoxRows) ||
-      !mk(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup) ||
-      !make_map_1d(&tmS, a->s2, w_ue, (uint64_t)pl.E * (pl.H / kGroup) * (pl.I / kGroup)))
-    return MOE_ERR_CUDA;
+  const bool small = pl.ws.small_batch != 0;
+  const uint64_t n_ws = (uint64_t)pl.E * (pl.H / kGroup) * (pl.I / kGroup);
+  constexpr uint32_t pk = TileCfg<false>::PK;
+  const bool maps_ok =
+      small ? make_map_u8(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kABoxRows) &&
+                  make_map_u8(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup) &&
+                  make_map_1d(&tmS, a->s2, w_ue, n_ws)
+            : make_map_act_tile(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, pk) &&
+                  make_map_u8_3d_pk(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kBN, pk) &&
+                  make_map_act_scales(&tmAS, at<void>(ws, pl.ws.a2_s), pl.act_fmt == MOE_SCALE_UE8M0,
+                                      pl.ws.R_cap, pl.I / kGroup, pk) &&
+                  make_map_1d(&tmS, a->s2, w_ue, n_ws, 32);
+  if (!maps_ok) return MOE_ERR_CUDA;
   GemmParams p;
   fill_gemm_common(p, pl, ws);
   p.tile_row0 = tile_row0;
@@ -354,14 +404,13 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.ksplit = 1;
   void* y = y_target != nullptr ? y_target : at<void>(ws, pl.ws.y);
   p.y = static_cast<uint16_t*>(y);
-  const bool small = pl.ws.small_batch != 0;
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
   CUtensorMap tmY;
   if (!small && !make_map_bf16_store(&tmY, y, pl.H, pl.ws.R_cap))
     return MOE_ERR_CUDA;
   const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
-                                : launch_fc2(tmA, tmB, tmS, tmY, p, grid, s);
+                                : launch_fc2(tmA, tmB, tmAS, tmS, tmY, p, grid, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -10,20 +10,24 @@
 //
 // Work item = (live row tile, output column block, K split).  One CTA per SM walks items
 // blockIdx.x, blockIdx.x + gridDim.x, ...; inside the CTA:
-//   warp 0 (one lane)  TMA producer.  Per 128-wide K block one stage of a 4-stage ring receives
-//                      the tile's live activation rows (8-row boxes, only those below the
-//                      expert's live end), 256 weight rows (128-byte swizzle), the 128 activation
-//                      scales of the K block (bulk copy) and the two weight block scales (16-byte
-//                      boxes of a 1-D tensor map), all counted on the stage's mbarrier.
+//   warp 0 (one lane)  TMA producer.  Each stage of the operand ring receives the tile's 128
+//                      activation rows (one 5-D box that also permutes the 8-row groups, below)
+//                      and its 256 weight rows (one box, 128-byte swizzle) for one or two 128-wide
+//                      K blocks; a separate, deeper ring of scale slots receives the stage's
+//                      activation scales (one 2-D box) and two 32-byte boxes of weight block
+//                      scales.  Five copies per stage.  The MMA releases an operand stage on
+//                      completion, the promotion warps release the scale slot once they have
+//                      read it.  Rows of a tile past the expert's live end are loaded too (they
+//                      stay inside the workspace) and their results are discarded.
 //   warp 1 (one lane)  MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) per K block
 //                      into one of two 256-column fp32 accumulators in tensor memory.
 //   warps 2..9         promotion + epilogue.  A thread owns one row and 128 of the 256 columns;
 //                      per K block it reads its partial sums from tensor memory and accumulates
 //                      acc = fma(partial, a_scale*b_scale, acc) in registers, then releases the
 //                      accumulator so the MMA of a later K block overlaps the promotion.
-// Row placement: activation rows are loaded in 8-row groups; group j goes to tensor-memory lanes
-// 32*(j%4) + 8*(j/4) .. +7, so even a tile with 8..32 live rows keeps all four lane quarters (all
-// eight promotion warps) busy.
+// Row placement: 8-row group j = 4a + b of the tile (rows 32a + 8b ..) lands in shared-memory group
+// 4b + a, i.e. tensor-memory lanes 32b + 8a .. +7, so even a tile with 8..32 live rows keeps all
+// four lane quarters (all eight promotion warps) busy.
 // FC1 columns: 128 gate rows of W13 and the matching 128 up rows, so a thread owns 64 (gate, up)
 // pairs of one row; the SwiGLU and the 1x128 requantization need only the row amax of the two
 // threads sharing the row.  FC2 columns: 256 consecutive hidden columns, BF16 out.
@@ -107,8 +111,8 @@ __device__ __forceinline__ void promote32(uint32_t taddr, float sab, float* acc)
 template <bool kFC1>
 __global__ void __launch_bounds__(kTileThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmS, const __grid_constant__ CUtensorMap tmY,
-                   const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmAS, const __grid_constant__ CUtensorMap tmS,
+                   const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
   using TC = TileCfg<kFC1>;
   constexpr int kPK = TC::PK;
   constexpr int kStages = TC::Stages;
@@ -116,22 +120,28 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   constexpr int kABytes = TC::ABytes;
   constexpr int kBHalfBytes = TC::BHalf;
   constexpr int kScaleSlotBytes = TC::SlotBytes;
+  constexpr int kSlots = TC::ScaleSlots;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_base = smem_addr(smem_raw);
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_base);
   uint8_t* ystage = smem + kStages * kStageBytes;              // FC2 output staging, 1024-aligned
   uint8_t* slots = ystage + 8 * TC::YWarpBytes;                 // scale slots, 128-byte aligned
-  uint8_t* ctrl = slots + kStages * kScaleSlotBytes;
+  uint8_t* ctrl = slots + kSlots * kScaleSlotBytes;
   const uint32_t slot0 = smem_addr(slots);
   const uint32_t bar0 = smem_addr(ctrl);
-  // barriers: full[kStages], empty[kStages], tfull[2], tempty[2], drain
+  // barriers: full[kStages], empty[kStages], sfull[kSlots], sempty[kSlots], tfull[2], tempty[2],
+  // drain
+  constexpr int kBarT = 2 * kStages + 2 * kSlots;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kStages + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kStages + 2 + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kStages + 4);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kStages + 5));
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * kStages + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (2 * kStages + kSlots + i); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (kBarT + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (kBarT + 2 + b); };
+  const uint32_t drain_bar = bar0 + 8u * (kBarT + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (kBarT + 5));
+  static_assert(8 * (kBarT + 5) + 16 <= 1024, "barrier area");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* mma_consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
@@ -144,8 +154,11 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(full_bar(s), 1);
-      // a stage is free once the MMAs read it and every promotion warp read its scales
-      mbar_init(empty_bar(s), 1 + kEpiWarps);
+      mbar_init(empty_bar(s), 1);            // the MMAs have read the operands
+    }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(sfull_bar(i), 1);
+      mbar_init(sempty_bar(i), kEpiWarps);   // every promotion warp has read the scales
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -160,6 +173,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   if (warp == 0 && lane == 0) {
     prefetch_tensormap(&tmA);
     prefetch_tensormap(&tmB);
+    prefetch_tensormap(&tmAS);
     prefetch_tensormap(&tmS);
   }
   if (warp == 1) tmem_alloc(smem_addr(tmem_slot), kTmemCols);
@@ -175,8 +189,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const int KB = p.K / kBK;
   const int kb_per_split = KB / p.ksplit;
   const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
-  const int a_scale_bytes = a_ue ? kBM : kBM * 4;
-  const int w_per16 = b_ue ? 16 : 4;      // scale elements per 16-byte box
+  const int a_kb_bytes = a_ue ? kBM : kBM * 4;   // activation scales of one K block in a slot
+  const int w_per16 = b_ue ? 16 : 4;             // scale elements per 16 bytes
   int* status = p.status;
 
   const int nst_item = (kb_per_split + kPK - 1) / kPK;   // pipeline stages per work item
@@ -191,56 +205,43 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     const uint64_t pol_w = policy_evict_first();
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Item w = decode_item(p, item);
-      const int nbox = (w.live + kABoxRows - 1) / kABoxRows;
-      int brow0, brow1;
-      bool second;
-      if (kFC1) {
-        brow0 = w.e * p.b_rows_per_expert + w.nb * kGroup;                  // gate rows
-        brow1 = brow0 + p.out_cols;                                         // matching up rows
-        second = true;
-      } else {
-        brow0 = w.e * p.b_rows_per_expert + w.nb * kBN;
-        brow1 = brow0 + kGroup;
-        second = (w.nb * kBN + kGroup) < p.out_cols;
-      }
+      // FC1: 128 gate rows and the matching 128 up rows (the map's outer dimension steps I rows);
+      // FC2: 256 consecutive hidden rows (past the expert's last block they are never used)
+      const int brow0 = kFC1 ? w.e * p.b_rows_per_expert + w.nb * kGroup
+                             : w.e * p.b_rows_per_expert + w.nb * kBN;
       int sr0, sr1;
       bool has_sr1;
       scale_rows<kFC1>(p, w, sr0, sr1, has_sr1);
       const int kb_end = (w.ks + 1) * kb_per_split;
       for (int st = 0; st < nst_item; ++st) {
         const int kbs = w.ks * kb_per_split + st * kPK;       // first K block of the stage
-        const int nv = min(kPK, kb_end - kbs);                // K blocks of the stage that exist
         const int s = sc % kStages;
         const uint32_t ph = (sc / kStages) & 1;
-        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) {
+        const int sl = sc % kSlots;
+        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status) ||
+            !mbar_wait(sempty_bar(sl), ((sc / kSlots) & 1) ^ 1, abort_flag, status)) {
           ok = false;
           break;
         }
-        // boxes always deliver kPK K blocks (past the end of K they read as zero)
-        const uint32_t bytes = nbox * (kABoxRows * kBK * kPK) + (second ? 2 : 1) * kBHalfBytes +
-                               nv * (a_scale_bytes + (has_sr1 ? 32 : 16));
-        mbar_arrive_expect_tx(full_bar(s), bytes);
+        // every box is delivered whole (kPK K blocks; past the end of a dimension as zeros)
+        mbar_arrive_expect_tx(full_bar(s), kABytes + 2 * kBHalfBytes);
+        mbar_arrive_expect_tx(sfull_bar(sl), kPK * a_kb_bytes + (has_sr1 ? 64 : 32));
         const uint32_t sA = sbase + s * kStageBytes;
         const uint32_t sB = sA + kABytes;
-        const uint32_t sS = slot0 + s * kScaleSlotBytes;
-        // 8-row group j of the tile -> smem group 4*(j%4) + j/4, i.e. TMEM lanes 32*(j%4) + 8*(j/4)
-        for (int j = 0; j < nbox; ++j)
-          tma_load_3d(sA + (4 * (j & 3) + (j >> 2)) * (kABoxRows * kBK * kPK), &tmA, 0,
-                      w.m0 + j * kABoxRows, kbs, full_bar(s));
-        tma_load_3d_hint(sB, &tmB, 0, brow0, kbs, full_bar(s), pol_w);
-        if (second) tma_load_3d_hint(sB + kBHalfBytes, &tmB, 0, brow1, kbs, full_bar(s), pol_w);
-        for (int k = 0; k < nv; ++k) {
-          const int kb = kbs + k;
-          bulk_copy_g2s(sS + k * kSlotAScale,
-                        static_cast<const uint8_t*>(p.a_scale) +
-                            ((size_t)kb * p.R_cap + w.m0) * (a_ue ? 1 : 4),
-                        a_scale_bytes, full_bar(s));
-          const int i0 = sr0 * KB + kb;
-          tma_load_1d(sS + kSlotW + k * kSlotWStride, &tmS, i0 - i0 % w_per16, full_bar(s));
-          if (has_sr1) {
-            const int i1 = sr1 * KB + kb;
-            tma_load_1d(sS + kSlotW + k * kSlotWStride + 128, &tmS, i1 - i1 % w_per16, full_bar(s));
-          }
+        const uint32_t sS = slot0 + sl * kScaleSlotBytes;
+        tma_load_5d(sA, &tmA, 0, 0, kbs, w.m0 / 32, 0, full_bar(s));
+        if (kFC1)
+          tma_load_4d_hint(sB, &tmB, 0, brow0, kbs, 0, full_bar(s), pol_w);
+        else
+          tma_load_3d_hint(sB, &tmB, 0, brow0, kbs, full_bar(s), pol_w);
+        tma_load_2d(sS, &tmAS, w.m0, kbs, sfull_bar(sl));
+        // a 32-byte box from the 16-byte boundary at or below the stage's first block scale
+        // holds the scales of all kPK K blocks
+        const int i0 = sr0 * KB + kbs;
+        tma_load_1d(sS + kSlotW, &tmS, i0 - i0 % w_per16, sfull_bar(sl));
+        if (has_sr1) {
+          const int i1 = sr1 * KB + kbs;
+          tma_load_1d(sS + kSlotW + 128, &tmS, i1 - i1 % w_per16, sfull_bar(sl));
         }
         ++sc;
       }
@@ -313,23 +314,21 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       for (int st = 0; ok && st < nst_item; ++st) {
         const int kbs = w.ks * kb_per_split + st * kPK;
         const int nv = min(kPK, kb_end - kbs);
-        const int s = sc % kStages;
-        const uint8_t* slot = slots + s * kScaleSlotBytes;
+        const int sl = sc % kSlots;
+        const uint8_t* slot = slots + sl * kScaleSlotBytes;
         for (int k = 0; k < nv; ++k) {
           const int b = c & 1;
           if (!mbar_wait(tfull_bar(b), (c >> 1) & 1, abort_flag, status) ||
-              (k == 0 && !mbar_wait(full_bar(s), (sc / kStages) & 1, abort_flag, status))) {
+              (k == 0 && !mbar_wait(sfull_bar(sl), (sc / kSlots) & 1, abort_flag, status))) {
             ok = false;
             break;
           }
-          const int kb = kbs + k;
           float sab0 = 0.0f, sab1 = 0.0f;
           if (qlive) {
-            const float sa = smem_scale_at(slot + k * kSlotAScale, row, a_ue);
-            const int i0 = sr0 * KB + kb, i1 = sr1 * KB + kb;
-            const float sw0 = smem_scale_at(slot + kSlotW + k * kSlotWStride, i0 % w_per16, b_ue);
-            const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotW + k * kSlotWStride + 128,
-                                                      i1 % w_per16, b_ue)
+            const float sa = smem_scale_at(slot + k * a_kb_bytes, row, a_ue);
+            const int i0 = sr0 * KB + kbs, i1 = sr1 * KB + kbs;
+            const float sw0 = smem_scale_at(slot + kSlotW, i0 % w_per16 + k, b_ue);
+            const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotW + 128, i1 % w_per16 + k, b_ue)
                                       : 0.0f;
             sab0 = __fmul_rn(sa, sw0);
             sab1 = __fmul_rn(sa, sw1);
@@ -357,7 +356,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         }
         if (!ok) break;
         __syncwarp();
-        if (lane == 0) mbar_arrive(empty_bar(s));   // this warp has read the stage's scales
+        if (lane == 0) mbar_arrive(sempty_bar(sl));   // this warp has read the stage's scales
         ++sc;
       }
       if (!ok) break;
@@ -514,6 +513,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // stages issued but never consumed are still in flight: wait for them before leaving
     for (int st = *mma_consumed; st < prod_issued; ++st)
       drain_wait(full_bar(st % kStages), (st / kStages) & 1, status);
+    // scale copies: the latest use of each slot (earlier uses completed before it was reissued)
+    for (int st = max(0, prod_issued - kSlots); st < prod_issued; ++st)
+      drain_wait(sfull_bar(st % kSlots), (st / kSlots) & 1, status);
   }
   tc_fence_before_sync();
   __syncthreads();
@@ -524,24 +526,26 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 }
 
 template <bool kFC1>
-static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                               const CUtensorMap& tmY, const GemmParams& p, int grid, cudaStream_t s) {
+static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
+                               const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p,
+                               int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<kFC1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TileCfg<kFC1>::Smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(k_grouped_gemm<kFC1>, dim3(grid), dim3(kTileThreads), TileCfg<kFC1>::Smem, s, tmA,
-                    tmB, tmS, tmY, p);
+                    tmB, tmAS, tmS, tmY, p);
 }
 
-cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                       const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_gemm<true>(tmA, tmB, tmS, tmA, p, grid, s);   // FC1 stores no BF16 tile
+cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
+                       const CUtensorMap& tmS, const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm<true>(tmA, tmB, tmAS, tmS, tmA, p, grid, s);   // FC1 stores no BF16 tile
 }
 
-cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                       const CUtensorMap& tmY, const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_gemm<false>(tmA, tmB, tmS, tmY, p, grid, s);
+cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
+                       const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p, int grid,
+                       cudaStream_t s) {
+  return launch_gemm<false>(tmA, tmB, tmAS, tmS, tmY, p, grid, s);
 }
 
 }  // namespace moe

@@ -39,7 +39,10 @@ constexpr int kSTmemBufs = 4;
 constexpr int kSBufCols = 2 * kSN;            // gate/up (or block 0/1) x 32 tokens
 constexpr int kSTmemCols = kSTmemBufs * kSBufCols;
 constexpr int kSThreads = 320;
-constexpr int kSSmemBytes = kSStages * (kSStageBytes + kSSlotBytes) + 1024 /*align*/ +
+// scale slots have their own ring: an operand stage is released when its MMAs complete, the
+// scales when all promotion warps have read them (they trail the MMA by up to kSTmemBufs K blocks)
+constexpr int kSSlots = kSStages + kSTmemBufs;
+constexpr int kSSmemBytes = kSStages * kSStageBytes + kSSlots * kSSlotBytes + 1024 /*align*/ +
                             1024 /*bars*/ + 2 * 4 * kSN * 4 /*token amax exchange*/;
 constexpr uint32_t kSIdesc = make_idesc_e4m3(kGroup, kSN);
 
@@ -104,15 +107,20 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const uint32_t sbase = (raw_base + 1023u) & ~1023u;
   uint8_t* smem = smem_raw + (sbase - raw_base);
   uint8_t* slots = smem + kSStages * kSStageBytes;
-  uint8_t* ctrl = slots + kSStages * kSSlotBytes;
+  uint8_t* ctrl = slots + kSSlots * kSSlotBytes;
   const uint32_t slot0 = smem_addr(slots);
   const uint32_t bar0 = smem_addr(ctrl);
+  // barriers: full/empty[kSStages], sfull/sempty[kSSlots], tfull/tempty[kSTmemBufs], drain
+  constexpr int kBarT = 2 * kSStages + 2 * kSSlots;
   auto full_bar = [&](int s) { return bar0 + 8u * s; };
   auto empty_bar = [&](int s) { return bar0 + 8u * (kSStages + s); };
-  auto tfull_bar = [&](int b) { return bar0 + 8u * (2 * kSStages + b); };
-  auto tempty_bar = [&](int b) { return bar0 + 8u * (2 * kSStages + kSTmemBufs + b); };
-  const uint32_t drain_bar = bar0 + 8u * (2 * kSStages + 2 * kSTmemBufs);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (2 * kSStages + 2 * kSTmemBufs + 1));
+  auto sfull_bar = [&](int i) { return bar0 + 8u * (2 * kSStages + i); };
+  auto sempty_bar = [&](int i) { return bar0 + 8u * (2 * kSStages + kSSlots + i); };
+  auto tfull_bar = [&](int b) { return bar0 + 8u * (kBarT + b); };
+  auto tempty_bar = [&](int b) { return bar0 + 8u * (kBarT + kSTmemBufs + b); };
+  const uint32_t drain_bar = bar0 + 8u * (kBarT + 2 * kSTmemBufs);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ctrl + 8 * (kBarT + 2 * kSTmemBufs + 1));
+  static_assert(8 * (kBarT + 2 * kSTmemBufs + 1) + 16 <= 1024, "barrier area");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* mma_consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
   volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
@@ -125,7 +133,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < kSStages; ++s) {
       mbar_init(full_bar(s), 1);
-      mbar_init(empty_bar(s), 1 + kEpiWarps);
+      mbar_init(empty_bar(s), 1);
+    }
+    for (int i = 0; i < kSSlots; ++i) {
+      mbar_init(sfull_bar(i), 1);
+      mbar_init(sempty_bar(i), kEpiWarps);
     }
     for (int b = 0; b < kSTmemBufs; ++b) {
       mbar_init(tfull_bar(b), 1);
@@ -183,32 +195,35 @@ __global__ void __launch_bounds__(kSThreads, 1)
         sr1 = sr0 + 1;
         second = 2 * w.nb + 1 < ncb;
       }
-      const uint32_t bytes = (second ? 2 : 1) * (kGroup * kBK) + nbox * (kABoxRows * kBK) +
-                             a_scale_bytes + (second ? 32 : 16);
+      const uint32_t bytes = (second ? 2 : 1) * (kGroup * kBK) + nbox * (kABoxRows * kBK);
+      const uint32_t sbytes = a_scale_bytes + (second ? 32 : 16);
       const int kb0 = w.ks * kb_per_split;
       for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
         const int s = it % kSStages;
         const uint32_t ph = (it / kSStages) & 1;
-        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status)) {
+        const int sl = it % kSSlots;
+        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status) ||
+            !mbar_wait(sempty_bar(sl), ((it / kSSlots) & 1) ^ 1, abort_flag, status)) {
           ok = false;
           break;
         }
         mbar_arrive_expect_tx(full_bar(s), bytes);
+        mbar_arrive_expect_tx(sfull_bar(sl), sbytes);
         const uint32_t sW = sbase + s * kSStageBytes;
         const uint32_t sX = sW + kSWBytes;
-        const uint32_t sS = slot0 + s * kSSlotBytes;
+        const uint32_t sS = slot0 + sl * kSSlotBytes;
         tma_load_2d_hint(sW, &tmB, kb * kBK, brow0, full_bar(s), pol_w);
         if (second) tma_load_2d_hint(sW + kGroup * kBK, &tmB, kb * kBK, brow1, full_bar(s), pol_w);
         for (int j = 0; j < nbox; ++j)
           tma_load_2d(sX + j * (kABoxRows * kBK), &tmA, kb * kBK, w.row0 + j * kABoxRows, full_bar(s));
         bulk_copy_g2s(sS, static_cast<const uint8_t*>(p.a_scale) +
                               ((size_t)kb * p.R_cap + w.row0) * (a_ue ? 1 : 4),
-                      a_scale_bytes, full_bar(s));
+                      a_scale_bytes, sfull_bar(sl));
         const int i0 = sr0 * KB + kb;
-        tma_load_1d(sS + kSSlotW0, &tmS, i0 - i0 % w_per16, full_bar(s));
+        tma_load_1d(sS + kSSlotW0, &tmS, i0 - i0 % w_per16, sfull_bar(sl));
         if (second) {
           const int i1 = sr1 * KB + kb;
-          tma_load_1d(sS + kSSlotW1, &tmS, i1 - i1 % w_per16, full_bar(s));
+          tma_load_1d(sS + kSSlotW1, &tmS, i1 - i1 % w_per16, sfull_bar(sl));
         }
         ++it;
       }
@@ -272,16 +287,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
       for (int c = 0; c < 16; ++c) acc0[c] = acc1[c] = 0.0f;
       const int kb0 = w.ks * kb_per_split;
       for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
-        const int s = it % kSStages;
+        const int sl = it % kSSlots;
         const int b = it % kSTmemBufs;
         if (!mbar_wait(tfull_bar(b), (it / kSTmemBufs) & 1, abort_flag, status) ||
-            !mbar_wait(full_bar(s), (it / kSStages) & 1, abort_flag, status)) {
+            !mbar_wait(sfull_bar(sl), (it / kSSlots) & 1, abort_flag, status)) {
           ok = false;
           break;
         }
         tc_fence_after_sync();
         if (ntok > 0) {
-          const uint8_t* slot = slots + s * kSSlotBytes;
+          const uint8_t* slot = slots + sl * kSSlotBytes;
           const int i0 = sr0 * KB + kb, i1 = sr1 * KB + kb;
           const float sw0 = smem_scale_at(slot + kSSlotW0, i0 % w_per16, b_ue);
           const float sw1 = has1 ? smem_scale_at(slot + kSSlotW1, i1 % w_per16, b_ue) : 0.0f;
@@ -302,7 +317,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
         tc_fence_before_sync();
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(empty_bar(s));
+          mbar_arrive(sempty_bar(sl));
           mbar_arrive(tempty_bar(b));
         }
         ++it;
@@ -413,6 +428,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (warp == 0 && lane == 0 && *abort_flag) {
     for (int it = *mma_consumed; it < prod_issued; ++it)
       s_drain_wait(full_bar(it % kSStages), (it / kSStages) & 1, status);
+    // scale copies: the latest use of each slot (earlier uses completed before it was reissued)
+    for (int it = max(0, prod_issued - kSSlots); it < prod_issued; ++it)
+      s_drain_wait(sfull_bar(it % kSSlots), (it / kSSlots) & 1, status);
   }
   tc_fence_before_sync();
   __syncthreads();

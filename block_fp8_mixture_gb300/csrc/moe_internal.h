@@ -45,9 +45,10 @@ constexpr int kTmemCols = 512;                        // two 256-column accumula
 // Per-stage scale slot: [k*512, +512) the 128 activation scales of the stage's K block k (fp32 or
 // UE8M0 bytes); [1024 + k*256, +16) and [1024 + k*256 + 128, +16) the 16-byte aligned chunks
 // holding the two weight block scales of K block k.
-constexpr int kSlotAScale = 512;
+// tile-kernel scale slot: [K block][128 activation scales] at 0, the two 32-byte weight-scale
+// boxes (which cover the stage's K blocks) at kSlotW and kSlotW + 128
 constexpr int kSlotW = 1024;
-constexpr int kSlotWStride = 256;
+constexpr int kSlotBytes = kSlotW + 256;
 constexpr int kMaxPK = 2;
 
 // Pipeline shape of the 128-row-tile kernel.  FC1 (long K, small output) streams two K blocks per
@@ -61,9 +62,13 @@ struct TileCfg {
   static constexpr int ABytes = kBM * kBK * PK;
   static constexpr int BHalf = kGroup * kBK * PK;     // 128 weight rows
   static constexpr int StageBytes = ABytes + 2 * BHalf;
-  static constexpr int SlotBytes = kSlotW + PK * kSlotWStride;
+  static constexpr int SlotBytes = kSlotBytes;
+  static_assert(PK * kBM * 4 <= kSlotW, "activation scales of a stage fit the slot");
+  // scale slots form their own ring, deeper than the operand ring: an operand stage is released
+  // as soon as the MMAs have read it, while the promotion warps still read the stage's scales
+  static constexpr int ScaleSlots = Stages + 2;
   static constexpr int YWarpBytes = kFC1 ? 0 : 8192;  // 32 rows x 128 BF16 columns per warp
-  static constexpr int Smem = Stages * StageBytes + Stages * SlotBytes + 8 * YWarpBytes +
+  static constexpr int Smem = Stages * StageBytes + ScaleSlots * SlotBytes + 8 * YWarpBytes +
                               1024 /*align*/ + 1024 /*bars*/ + 2 * kBM * 4 /*row amax*/;
 };
 static_assert(TileCfg<true>::Smem <= 232448 && TileCfg<false>::Smem <= 232448, "shared memory");
@@ -200,10 +205,13 @@ cudaError_t launch_align(const AlignParams& p, cudaStream_t s);
 cudaError_t launch_batch_prep(const BatchPrepParams& p, cudaStream_t s);
 cudaError_t launch_quant_rows(const QuantRowsParams& p, cudaStream_t s);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
-cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                       const GemmParams& p, int grid, cudaStream_t s);
-cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
-                       const CUtensorMap& tmY, const GemmParams& p, int grid, cudaStream_t s);
+// tile kernel maps: tmA activation rows (5-D), tmB weight rows, tmAS activation scales (2-D),
+// tmS weight block scales (1-D, 32-byte boxes), tmY the BF16 output (FC2)
+cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
+                       const CUtensorMap& tmS, const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
+                       const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p, int grid,
+                       cudaStream_t s);
 cudaError_t launch_fc1_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                              const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc2_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
