@@ -368,7 +368,9 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks * p.ksplit;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
+  const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
   const cudaError_t err = small ? launch_fc1_small(tmA, tmB, tmS, p, grid, s)
+                          : bs  ? launch_fc1_bs(tmA, tmB, tmAS, tmS, p, grid, s)
                                 : launch_fc1(tmA, tmB, tmAS, tmS, p, grid, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -409,7 +411,9 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   CUtensorMap tmY;
   if (!small && !make_map_bf16_store(&tmY, y, pl.H, pl.ws.R_cap))
     return MOE_ERR_CUDA;
+  const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
   const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
+                          : bs  ? launch_fc2_bs(tmA, tmB, tmAS, tmS, tmY, p, grid, s)
                                 : launch_fc2(tmA, tmB, tmAS, tmS, tmY, p, grid, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

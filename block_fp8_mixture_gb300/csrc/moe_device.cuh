@@ -259,6 +259,45 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
                : "memory");
 }
 
+// D[tmem] (+)= (A * 2^sfa)[smem] * (B * 2^sfb)[smem]^T: kind::mxf8f6f4 with UE8M0 scale factors
+// in tensor memory, one per 32-element K block of every row of A (sfa: lane = row) and of every
+// row of B (sfb: lane = row), issued by one thread.
+__device__ __forceinline__ void mma_f8_bs(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;"
+      "\n\t}" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+      : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with block scaling: A and B E4M3, both K-major, UE8M0
+// scale factors taken from byte 0 of their tensor-memory words, shape M x N (D is fp32).
+__host__ __device__ constexpr uint32_t make_idesc_mx_e4m3(int M, int N) {
+  return (0u << 4)                            // B scale factor: byte 0
+         | (0u << 7) | (0u << 10)             // A, B format: E4M3
+         | (0u << 15) | (0u << 16)            // A, B K-major
+         | ((uint32_t)(N >> 3) << 17)         // N / 8
+         | (1u << 23)                         // scale factor type: UE8M0
+         | ((uint32_t)(M >> 4) << 24)         // M / 16
+         | (0u << 29);                        // A scale factor: byte 0
+}
+
+// Four consecutive 32-bit tensor-memory columns of this warp's 32 lanes from registers.
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2,
+                                         uint32_t v3) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr),
+               "r"(v0), "r"(v1), "r"(v2), "r"(v3)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 // Instruction descriptor of kind::f8f6f4: D fp32, A and B E4M3, both K-major, shape M x N.
 __host__ __device__ constexpr uint32_t make_idesc_e4m3(int M, int N) {
   return (1u << 4)                            // D format: fp32

@@ -33,72 +33,11 @@
 // threads sharing the row.  FC2 columns: 256 consecutive hidden columns, BF16 out.
 // Small batches split K across CTAs (FC1 only): each split writes its fp32 partial rows, the last
 // split to arrive (atomic counter per item) sums the splits in fixed order and runs the epilogue.
-#include "moe_device.cuh"
+#include "moe_tile.cuh"
 
 namespace moe {
 
 constexpr uint32_t kIdesc = make_idesc_e4m3(kBM, kGroup);   // M = 128, N = 128 per MMA
-
-struct Item {
-  int tile, nb, ks, e, m0, live;
-};
-
-__device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
-  Item it;
-  const int per_tile = p.n_blocks * p.ksplit;
-  it.tile = item / per_tile;
-  const int rem = item - it.tile * per_tile;
-  it.nb = rem / p.ksplit;
-  it.ks = rem - it.nb * p.ksplit;
-  // tiles are contiguous from row 0 (routed layer) or listed (batched-expert layout)
-  it.m0 = p.tile_row0 != nullptr ? p.tile_row0[it.tile] : it.tile * kBM;
-  it.e = p.tile_expert[it.m0 / kBM];
-  it.live = min(kBM, p.live_end[it.e] - it.m0);
-  return it;
-}
-
-// Weight block-scale rows of an item (indices into the [E][row blocks][K/128] scale array).
-// FC1: the gate block nb and the up block I/128 + nb.  FC2: hidden blocks 2nb and 2nb + 1.
-template <bool kFC1>
-__device__ __forceinline__ void scale_rows(const GemmParams& p, const Item& w, int& r0, int& r1,
-                                           bool& has_r1) {
-  const int ncb = p.b_rows_per_expert / kGroup;
-  if (kFC1) {
-    r0 = w.e * ncb + w.nb;
-    r1 = w.e * ncb + p.out_cols / kGroup + w.nb;
-    has_r1 = true;
-  } else {
-    r0 = w.e * ncb + 2 * w.nb;
-    r1 = r0 + 1;
-    has_r1 = 2 * w.nb + 1 < ncb;
-  }
-}
-
-// SiLU(g) * u with the optional clamp, fp32, IEEE division, no fused multiply-add.
-__device__ __forceinline__ float swiglu(float g, float u, int mode, float lim) {
-  if (mode == MOE_CLAMP_BEFORE_SILU) {
-    g = fminf(g, lim);
-    u = fminf(fmaxf(u, -lim), lim);
-  }
-  const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-g)));   // correctly rounded 1/(1+e^-g)
-  float silu = __fmul_rn(g, sig);
-  if (mode == MOE_CLAMP_AFTER_SILU) {
-    silu = fminf(silu, lim);
-    u = fminf(fmaxf(u, -lim), lim);
-  }
-  return __fmul_rn(silu, u);
-}
-
-// Bounded wait used while tearing down: ignores the abort flag.
-__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
-  const uint64_t t0 = global_timer_ns();
-  while (!mbar_try_wait(bar, parity)) {
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
-      atomicCAS(status, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
-      return;
-    }
-  }
-}
 
 __device__ __forceinline__ void promote32(uint32_t taddr, float sab, float* acc) {
   uint32_t r[32];
@@ -362,141 +301,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       if (!ok) break;
 
       if (kFC1) {
-        const int I = p.out_cols;
-        if (p.ksplit > 1) {
-          // split-K fix-up: publish this split's partial rows, the last split sums all of them
-          const int pair = rlive ? p.sorted_pair[w.m0 + row] : 0;
-          if (rlive) {
-            float* dst = p.splitk_partial + ((size_t)w.ks * p.P_cap + pair) * (2 * I);
-#pragma unroll
-            for (int i = 0; i < 64; i += 4) {
-              *reinterpret_cast<float4*>(dst + w.nb * kGroup + wg * 64 + i) =
-                  make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-              *reinterpret_cast<float4*>(dst + I + w.nb * kGroup + wg * 64 + i) =
-                  make_float4(acc[64 + i], acc[65 + i], acc[66 + i], acc[67 + i]);
-            }
-          }
-          __threadfence();
-          named_barrier_sync(1, kEpiThreads);
-          if (ew == 0 && lane == 0) {
-            const int prev = atomicAdd(&p.splitk_count[w.tile * p.n_blocks + w.nb], 1);
-            *last_flag = (prev == p.ksplit - 1);
-          }
-          named_barrier_sync(1, kEpiThreads);
-          const bool last = *last_flag != 0;
-          named_barrier_sync(1, kEpiThreads);
-          if (!last) continue;
-          __threadfence();
-          if (ew == 0 && lane == 0) p.splitk_count[w.tile * p.n_blocks + w.nb] = 0;
-          if (rlive) {
-#pragma unroll
-            for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-            for (int s = 0; s < p.ksplit; ++s) {
-              const float* src = p.splitk_partial + ((size_t)s * p.P_cap + pair) * (2 * I);
-#pragma unroll
-              for (int i = 0; i < 64; i += 4) {
-                const float4 g = __ldcg(reinterpret_cast<const float4*>(src + w.nb * kGroup + wg * 64 + i));
-                const float4 u = __ldcg(reinterpret_cast<const float4*>(src + I + w.nb * kGroup + wg * 64 + i));
-                acc[i] = __fadd_rn(acc[i], g.x);
-                acc[i + 1] = __fadd_rn(acc[i + 1], g.y);
-                acc[i + 2] = __fadd_rn(acc[i + 2], g.z);
-                acc[i + 3] = __fadd_rn(acc[i + 3], g.w);
-                acc[64 + i] = __fadd_rn(acc[64 + i], u.x);
-                acc[65 + i] = __fadd_rn(acc[65 + i], u.y);
-                acc[66 + i] = __fadd_rn(acc[66 + i], u.z);
-                acc[67 + i] = __fadd_rn(acc[67 + i], u.w);
-              }
-            }
-          }
-        }
-        // SwiGLU on the BF16-rounded FC1 outputs, then 1x128 requantization over the row's 128
-        // (gate, up) columns held by this thread (64) and its partner in the other half (64).
-        float amax = 0.0f;
-        if (rlive) {
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            float h = swiglu(bf16_round(acc[i]), bf16_round(acc[64 + i]), p.clamp_mode,
-                             p.clamp_limit);
-            if (p.numerics == MOE_NUMERICS_RECIPROCAL) h = bf16_round(h);
-            acc[i] = h;
-            amax = fmaxf(amax, fabsf(h));
-          }
-        }
-        red[wg * kBM + row] = amax;
-        named_barrier_sync(1, kEpiThreads);
-        amax = fmaxf(red[row], red[kBM + row]);
-        named_barrier_sync(1, kEpiThreads);
-        if (rlive) {
-          float inv;
-          const float s = group_scale_numerics(amax, p.act_fmt, p.numerics, &inv);
-          uint8_t* dst = p.a2_q + (size_t)(w.m0 + row) * I + w.nb * kGroup + wg * 64;
-#pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            uint32_t wd[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float* h = acc + v * 16 + j * 4;
-              wd[j] = cvt_e4m3x2(quant_div(h[0], s, inv), quant_div(h[1], s, inv)) |
-                      (cvt_e4m3x2(quant_div(h[2], s, inv), quant_div(h[3], s, inv)) << 16);
-            }
-            *reinterpret_cast<uint4*>(dst + v * 16) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-          }
-          if (wg == 0)
-            store_scale(p.a2_s, (size_t)w.nb * p.R_cap + w.m0 + row, s, p.act_fmt == MOE_SCALE_UE8M0);
-        }
+        if (!fc1_item_epilogue(p, w, acc, row, wg, ew, lane, rlive, red, last_flag)) continue;
       } else {
-        // BF16 tile out through TMA stores: this warp's rows come in four 8-row groups
-        // (rows 32*g + 8*q .. +7).  The warp writes its 32 x 128 block into its own 8 KB staging
-        // buffer as 128-byte-swizzled 8 x 64 boxes and lane 0 issues the box stores without waiting
-        // for them; the buffer is reused one item later, after the stores have read it.  Groups
-        // that are only partly live (the end of an expert's rows) are written row by row instead.
-        const int col0 = w.nb * kBN + wg * kGroup;
-        if (qlive && col0 < p.out_cols) {
-          uint8_t* buf = ystage + ew * TC::YWarpBytes;
-          const uint32_t buf_s = smem_addr(buf);
-          const int t = lane & 7;
-          const int g_mine = lane >> 3;
-          const int grow_mine = 32 * g_mine + 8 * q;
-          if (lane == 0) bulk_wait_group_read0();     // the previous item's stores have read it
-          __syncwarp();
-          if (grow_mine + 8 <= w.live) {
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              uint32_t wd[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                wd[j] = f32_to_bf16_bits(acc[c * 8 + 2 * j]) |
-                        (f32_to_bf16_bits(acc[c * 8 + 2 * j + 1]) << 16);
-              const int box = c >> 3, cc = c & 7;
-              *reinterpret_cast<uint4*>(buf + g_mine * 2048 + box * 1024 + t * 128 + ((cc ^ t) << 4)) =
-                  make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            }
-          } else if (rlive) {
-            uint16_t* dst = p.y + (size_t)(w.m0 + row) * p.out_cols + col0;
-#pragma unroll
-            for (int v = 0; v < 16; ++v) {
-              uint32_t wd[4];
-#pragma unroll
-              for (int j = 0; j < 4; ++j)
-                wd[j] = f32_to_bf16_bits(acc[v * 8 + 2 * j]) |
-                        (f32_to_bf16_bits(acc[v * 8 + 2 * j + 1]) << 16);
-              *reinterpret_cast<uint4*>(dst + v * 8) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
-            }
-          }
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-#pragma unroll
-            for (int g = 0; g < 4; ++g) {
-              const int grow = 32 * g + 8 * q;
-              if (grow + 8 <= w.live) {
-                tma_store_2d(&tmY, col0, w.m0 + grow, buf_s + g * 2048);
-                tma_store_2d(&tmY, col0 + 64, w.m0 + grow, buf_s + g * 2048 + 1024);
-              }
-            }
-            bulk_commit_group();
-          }
-        }
+        fc2_item_epilogue(p, w, acc, row, wg, q, lane, qlive, rlive, ystage + ew * TC::YWarpBytes,
+                          &tmY);
       }
     }
   }

@@ -212,6 +212,12 @@ cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUt
 cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
                        const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p, int grid,
                        cudaStream_t s);
+// the same tile GEMMs for UE8M0 activation and weight scales, on the block-scaled MMA
+cudaError_t launch_fc1_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
+                          const CUtensorMap& tmS, const GemmParams& p, int grid, cudaStream_t s);
+cudaError_t launch_fc2_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
+                          const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p,
+                          int grid, cudaStream_t s);
 cudaError_t launch_fc1_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                              const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc2_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
