@@ -39,12 +39,17 @@ namespace moe {
 
 constexpr uint32_t kIdesc = make_idesc_e4m3(kBM, kGroup);   // M = 128, N = 128 per MMA
 
-__device__ __forceinline__ void promote32(uint32_t taddr, float sab, float* acc) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
+// acc[0..63] += partial[t0 .. t0+31, t1 .. t1+31] * sab: both tensor-memory loads in flight before
+// the one wait, so a K block costs two load round trips instead of four.
+__device__ __forceinline__ void promote64(uint32_t t0, uint32_t t1, float sab, float* acc) {
+  uint32_t r0[32], r1[32];
+  tmem_ld32(t0, r0);
+  tmem_ld32(t1, r1);
   tmem_ld_wait();
 #pragma unroll
-  for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(r[i]), sab, acc[i]);
+  for (int i = 0; i < 32; ++i) acc[i] = fmaf(__uint_as_float(r0[i]), sab, acc[i]);
+#pragma unroll
+  for (int i = 0; i < 32; ++i) acc[32 + i] = fmaf(__uint_as_float(r1[i]), sab, acc[32 + i]);
 }
 
 template <bool kFC1>
@@ -276,16 +281,12 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           if (qlive) {
             const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
             if (kFC1) {
-              promote32(t0 + wg * 64, sab0, acc);
-              promote32(t0 + wg * 64 + 32, sab0, acc + 32);
-              promote32(t0 + kGroup + wg * 64, sab1, acc + 64);
-              promote32(t0 + kGroup + wg * 64 + 32, sab1, acc + 96);
+              promote64(t0 + wg * 64, t0 + wg * 64 + 32, sab0, acc);
+              promote64(t0 + kGroup + wg * 64, t0 + kGroup + wg * 64 + 32, sab1, acc + 64);
             } else {
               const float sab = wg == 0 ? sab0 : sab1;
-              promote32(t0 + wg * 128, sab, acc);
-              promote32(t0 + wg * 128 + 32, sab, acc + 32);
-              promote32(t0 + wg * 128 + 64, sab, acc + 64);
-              promote32(t0 + wg * 128 + 96, sab, acc + 96);
+              promote64(t0 + wg * 128, t0 + wg * 128 + 32, sab, acc);
+              promote64(t0 + wg * 128 + 64, t0 + wg * 128 + 96, sab, acc + 64);
             }
           }
           tc_fence_before_sync();
