@@ -109,21 +109,6 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Byte matrix [outer][inner] (row stride = inner bytes), boxes of box_outer rows x 128 bytes with
-// the 128-byte swizzle the MMA descriptors expect.
-static bool make_map_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
-                        uint32_t box_outer) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  const cuuint64_t dims[2] = {inner, outer};
-  const cuuint64_t strides[1] = {inner};
-  const cuuint32_t box[2] = {(cuuint32_t)kBK, box_outer};
-  const cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Byte matrix [outer][inner] seen as 3-D (x = 128 bytes of a K block, y = row, z = K block), boxes of
 // box_outer rows x kPK K blocks: each row of a box is one kPK*128-byte contiguous run.
 static bool make_map_u8_3d_pk(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer,
@@ -168,8 +153,9 @@ static bool make_map_act_tile(CUtensorMap* m, const void* base, uint64_t K, uint
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// W13 [E*2I][H] as 4-D (x, row, K block, half with a stride of I rows): one box {128, 128, pk, 2}
-// brings 128 gate rows and the matching 128 up rows.
+// Weight rows [rows][K] as 4-D (x, row, K block, half with a stride of `half_rows` rows): one box
+// {128, 128, pk, 2} brings two 128-row blocks for pk K blocks, laid out [half][K block][row]
+// (FC1: 128 gate rows and the matching up rows, half_rows = I; FC2: 256 consecutive rows).
 static bool make_map_w13_tile(CUtensorMap* m, const void* base, uint64_t H, uint64_t rows,
                               uint64_t I, uint32_t pk) {
   EncodeTiledFn fn = encode_fn();
@@ -177,6 +163,21 @@ static bool make_map_w13_tile(CUtensorMap* m, const void* base, uint64_t H, uint
   const cuuint64_t dims[4] = {(cuuint64_t)kBK, rows, H / kBK, 2};
   const cuuint64_t strides[3] = {H, (cuuint64_t)kBK, I * H};
   const cuuint32_t box[4] = {(cuuint32_t)kBK, (cuuint32_t)kGroup, pk, 2};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Token rows of the small-batch kernel [R][K] bytes as 4-D (x, row inside an 8-row group, K block,
+// 8-row group): one box {128, 8, pk, 4} at (0, 0, kb, row0/8) brings a 32-row chunk for pk K blocks,
+// laid out [group][K block][8 rows][128 bytes].
+static bool make_map_tok_chunk(CUtensorMap* m, const void* base, uint64_t K, uint64_t R, uint32_t pk) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[4] = {(cuuint64_t)kBK, 8, K / kBK, R / 8};
+  const cuuint64_t strides[3] = {K, (cuuint64_t)kBK, 8 * K};
+  const cuuint32_t box[4] = {(cuuint32_t)kBK, 8, pk, 4};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 4, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -339,8 +340,8 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   const uint64_t n_ws = (uint64_t)pl.E * (2 * pl.I / kGroup) * (pl.H / kGroup);
   constexpr uint32_t pk = TileCfg<true>::PK;
   const bool maps_ok =
-      small ? make_map_u8(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kABoxRows) &&
-                  make_map_u8(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, kGroup) &&
+      small ? make_map_tok_chunk(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kSmallPK) &&
+                  make_map_w13_tile(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, pl.I, kSmallPK) &&
                   make_map_1d(&tmS, a->s13, w_ue, n_ws)
             : make_map_act_tile(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, pk) &&
                   make_map_w13_tile(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, pl.I, pk) &&
@@ -384,8 +385,8 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   const uint64_t n_ws = (uint64_t)pl.E * (pl.H / kGroup) * (pl.I / kGroup);
   constexpr uint32_t pk = TileCfg<false>::PK;
   const bool maps_ok =
-      small ? make_map_u8(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kABoxRows) &&
-                  make_map_u8(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup) &&
+      small ? make_map_tok_chunk(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, kSmallPK) &&
+                  make_map_w13_tile(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kGroup, kSmallPK) &&
                   make_map_1d(&tmS, a->s2, w_ue, n_ws)
             : make_map_act_tile(&tmA, at<void>(ws, pl.ws.a2_q), pl.I, pl.ws.R_cap, pk) &&
                   make_map_u8_3d_pk(&tmB, a->w2, pl.I, (uint64_t)pl.E * pl.H, kBN, pk) &&

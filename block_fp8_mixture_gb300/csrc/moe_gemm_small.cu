@@ -9,10 +9,11 @@
 // lanes and makes the per-128-K promotion read 128 x 256 partial sums for a few live rows.  Here the
 // work item is a live 32-row chunk of one expert (from the alignment kernel's chunk list) x one
 // output block x one K split:
-//   warp 0 (one lane)  TMA producer: per 128-wide K block one stage of a 5-stage ring receives 2 x 128
-//                      weight rows (FC1: gate block and the matching up block; FC2: two 128-column
-//                      blocks of H), the chunk's live activation rows (8-row boxes), the chunk's 32
-//                      activation scales and the two weight block scales.
+//   warp 0 (one lane)  TMA producer.  Each stage of a 3-stage ring holds two 128-wide K blocks:
+//                      one copy brings 2 x 128 weight rows (FC1: gate block and the matching up
+//                      block; FC2: two 128-column blocks of H) as 256-byte runs per row, one copy
+//                      the chunk's 32 token rows.  A separate ring of per-K-block slots receives
+//                      the chunk's 32 activation scales and the two weight block scales.
 //   warp 1 (one lane)  MMA issuer: per K block 2 x 4 tcgen05.mma kind::f8f6f4 with M = 128 weight
 //                      rows, N = 32 tokens, K = 32, into one of four 64-column accumulators.
 //   warps 2..9         promotion + epilogue.  Warp (q, half) owns weight rows 32q..32q+31 (its TMEM
@@ -28,9 +29,11 @@
 namespace moe {
 
 constexpr int kSN = 32;                       // tokens per chunk (MMA N)
-constexpr int kSStages = 5;
-constexpr int kSWBytes = 2 * kGroup * kBK;    // 256 weight rows x 128 bytes
-constexpr int kSXBytes = kSN * kBK;           // 32 token rows x 128 bytes
+constexpr int kSPK = kSmallPK;                // K blocks per operand stage
+constexpr int kSStages = 3;
+constexpr int kSWHalf = kGroup * kBK * kSPK;  // 128 weight rows x kSPK K blocks
+constexpr int kSWBytes = 2 * kSWHalf;         // [half][K block][128 rows][128 bytes]
+constexpr int kSXBytes = kSN * kBK * kSPK;    // [8-row group][K block][8 rows][128 bytes]
 constexpr int kSStageBytes = kSWBytes + kSXBytes;
 constexpr int kSSlotBytes = 384;              // [0,128) act scales, [128,144) w0, [256,272) w1
 constexpr int kSSlotW0 = 128;
@@ -39,11 +42,13 @@ constexpr int kSTmemBufs = 4;
 constexpr int kSBufCols = 2 * kSN;            // gate/up (or block 0/1) x 32 tokens
 constexpr int kSTmemCols = kSTmemBufs * kSBufCols;
 constexpr int kSThreads = 320;
-// scale slots have their own ring: an operand stage is released when its MMAs complete, the
-// scales when all promotion warps have read them (they trail the MMA by up to kSTmemBufs K blocks)
-constexpr int kSSlots = kSStages + kSTmemBufs;
+// scale slots (one per K block) have their own ring: an operand stage is released when its MMAs
+// complete, the scales when all promotion warps have read them (they trail the MMA by up to
+// kSTmemBufs K blocks)
+constexpr int kSSlots = kSStages * kSPK + kSTmemBufs;
 constexpr int kSSmemBytes = kSStages * kSStageBytes + kSSlots * kSSlotBytes + 1024 /*align*/ +
                             1024 /*bars*/ + 2 * 4 * kSN * 4 /*token amax exchange*/;
+static_assert(kSSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kSIdesc = make_idesc_e4m3(kGroup, kSN);
 
 struct Chunk {
@@ -171,92 +176,106 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int ncb = p.b_rows_per_expert / kGroup;
   int* status = p.status;
 
-  int prod_issued = 0;
+  int prod_issued = 0, prod_scales = 0;
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ producer
-    int it = 0;
+    int sc = 0, it = 0;
     bool ok = true;
     const uint64_t pol_w = policy_evict_first();
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Chunk w = decode_chunk(p, item);
-      const int nbox = (w.live + kABoxRows - 1) / kABoxRows;
-      int brow0, brow1, sr0, sr1;
+      int brow0, sr0, sr1;
       bool second;
       if (kFC1) {
-        brow0 = w.e * p.b_rows_per_expert + w.nb * kGroup;
-        brow1 = brow0 + p.out_cols;
+        brow0 = w.e * p.b_rows_per_expert + w.nb * kGroup;   // gate rows; up rows I further
         sr0 = w.e * ncb + w.nb;
         sr1 = w.e * ncb + p.out_cols / kGroup + w.nb;
         second = true;
       } else {
         brow0 = w.e * p.b_rows_per_expert + w.nb * 2 * kGroup;
-        brow1 = brow0 + kGroup;
         sr0 = w.e * ncb + 2 * w.nb;
         sr1 = sr0 + 1;
         second = 2 * w.nb + 1 < ncb;
       }
-      const uint32_t bytes = (second ? 2 : 1) * (kGroup * kBK) + nbox * (kABoxRows * kBK);
       const uint32_t sbytes = a_scale_bytes + (second ? 32 : 16);
       const int kb0 = w.ks * kb_per_split;
-      for (int kb = kb0; kb < kb0 + kb_per_split; ++kb) {
-        const int s = it % kSStages;
-        const uint32_t ph = (it / kSStages) & 1;
-        const int sl = it % kSSlots;
-        if (!mbar_wait(empty_bar(s), ph ^ 1, abort_flag, status) ||
-            !mbar_wait(sempty_bar(sl), ((it / kSSlots) & 1) ^ 1, abort_flag, status)) {
+      for (int kbs = kb0; ok && kbs < kb0 + kb_per_split; kbs += kSPK) {
+        const int nv = min(kSPK, kb0 + kb_per_split - kbs);
+        const int s = sc % kSStages;
+        if (!mbar_wait(empty_bar(s), ((sc / kSStages) & 1) ^ 1, abort_flag, status)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(full_bar(s), bytes);
-        mbar_arrive_expect_tx(sfull_bar(sl), sbytes);
+        // whole boxes always arrive (kSPK K blocks, 32 token rows, both weight halves; rows past
+        // the end of the weights read as zero)
+        mbar_arrive_expect_tx(full_bar(s), kSStageBytes);
         const uint32_t sW = sbase + s * kSStageBytes;
-        const uint32_t sX = sW + kSWBytes;
-        const uint32_t sS = slot0 + sl * kSSlotBytes;
-        tma_load_2d_hint(sW, &tmB, kb * kBK, brow0, full_bar(s), pol_w);
-        if (second) tma_load_2d_hint(sW + kGroup * kBK, &tmB, kb * kBK, brow1, full_bar(s), pol_w);
-        for (int j = 0; j < nbox; ++j)
-          tma_load_2d(sX + j * (kABoxRows * kBK), &tmA, kb * kBK, w.row0 + j * kABoxRows, full_bar(s));
-        bulk_copy_g2s(sS, static_cast<const uint8_t*>(p.a_scale) +
-                              ((size_t)kb * p.R_cap + w.row0) * (a_ue ? 1 : 4),
-                      a_scale_bytes, sfull_bar(sl));
-        const int i0 = sr0 * KB + kb;
-        tma_load_1d(sS + kSSlotW0, &tmS, i0 - i0 % w_per16, sfull_bar(sl));
-        if (second) {
-          const int i1 = sr1 * KB + kb;
-          tma_load_1d(sS + kSSlotW1, &tmS, i1 - i1 % w_per16, sfull_bar(sl));
+        tma_load_4d_hint(sW, &tmB, 0, brow0, kbs, 0, full_bar(s), pol_w);
+        tma_load_4d(sW + kSWBytes, &tmA, 0, 0, kbs, w.row0 / 8, full_bar(s));
+        ++sc;
+        for (int k = 0; k < nv; ++k) {
+          const int kb = kbs + k;
+          const int sl = it % kSSlots;
+          if (!mbar_wait(sempty_bar(sl), ((it / kSSlots) & 1) ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(sfull_bar(sl), sbytes);
+          const uint32_t sS = slot0 + sl * kSSlotBytes;
+          bulk_copy_g2s(sS, static_cast<const uint8_t*>(p.a_scale) +
+                                ((size_t)kb * p.R_cap + w.row0) * (a_ue ? 1 : 4),
+                        a_scale_bytes, sfull_bar(sl));
+          const int i0 = sr0 * KB + kb;
+          tma_load_1d(sS + kSSlotW0, &tmS, i0 - i0 % w_per16, sfull_bar(sl));
+          if (second) {
+            const int i1 = sr1 * KB + kb;
+            tma_load_1d(sS + kSSlotW1, &tmS, i1 - i1 % w_per16, sfull_bar(sl));
+          }
+          ++it;
         }
-        ++it;
       }
     }
-    prod_issued = it;
+    prod_issued = sc;
+    prod_scales = it;
   } else if (warp == 1 && lane == 0) {
     // ---------------------------------------------------------------- MMA
-    int it = 0;
+    int sc = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-      for (int k = 0; k < kb_per_split; ++k) {
-        const int s = it % kSStages;
-        const int b = it % kSTmemBufs;
-        if (!mbar_wait(full_bar(s), (it / kSStages) & 1, abort_flag, status) ||
-            !mbar_wait(tempty_bar(b), ((it / kSTmemBufs) & 1) ^ 1, abort_flag, status)) {
+      const int kb0 = decode_chunk(p, item).ks * kb_per_split;
+      for (int kbs = kb0; ok && kbs < kb0 + kb_per_split; kbs += kSPK) {
+        const int nv = min(kSPK, kb0 + kb_per_split - kbs);
+        const int s = sc % kSStages;
+        if (!mbar_wait(full_bar(s), (sc / kSStages) & 1, abort_flag, status)) {
           ok = false;
           break;
         }
-        tc_fence_after_sync();
         const uint32_t sW = sbase + s * kSStageBytes;
-        const uint64_t xdesc = make_sdesc_sw128(sW + kSWBytes);
+        for (int k = 0; k < nv; ++k) {
+          const int b = it % kSTmemBufs;
+          if (!mbar_wait(tempty_bar(b), ((it / kSTmemBufs) & 1) ^ 1, abort_flag, status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          // token operand: 8-row groups 2 KB apart, K block k at +1 KB
+          const uint64_t xdesc = make_sdesc_sw128(sW + kSWBytes + k * (kABoxRows * kBK),
+                                                  kABoxRows * kBK * kSPK);
 #pragma unroll
-        for (int h = 0; h < 2; ++h) {
-          const uint32_t d = tmem_base + b * kSBufCols + h * kSN;
-          const uint64_t wdesc = make_sdesc_sw128(sW + h * (kGroup * kBK));
+          for (int h = 0; h < 2; ++h) {
+            const uint32_t d = tmem_base + b * kSBufCols + h * kSN;
+            const uint64_t wdesc = make_sdesc_sw128(sW + h * kSWHalf + k * (kGroup * kBK));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 32; ++kk)
-            mma_f8(d, wdesc + 2 * kk, xdesc + 2 * kk, kSIdesc, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 32; ++kk)
+              mma_f8(d, wdesc + 2 * kk, xdesc + 2 * kk, kSIdesc, kk > 0 ? 1u : 0u);
+          }
+          mma_commit(tfull_bar(b));
+          ++it;
         }
+        if (!ok) break;
         mma_commit(empty_bar(s));
-        mma_commit(tfull_bar(b));
-        ++it;
-        *mma_consumed = it;
+        ++sc;
+        *mma_consumed = sc;
       }
     }
   } else if (warp >= kEpiWarp0) {
@@ -426,10 +445,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     s_drain_wait(drain_bar, 0, status);
   }
   if (warp == 0 && lane == 0 && *abort_flag) {
-    for (int it = *mma_consumed; it < prod_issued; ++it)
-      s_drain_wait(full_bar(it % kSStages), (it / kSStages) & 1, status);
+    for (int st = *mma_consumed; st < prod_issued; ++st)
+      s_drain_wait(full_bar(st % kSStages), (st / kSStages) & 1, status);
     // scale copies: the latest use of each slot (earlier uses completed before it was reissued)
-    for (int it = max(0, prod_issued - kSSlots); it < prod_issued; ++it)
+    for (int it = max(0, prod_scales - kSSlots); it < prod_scales; ++it)
       s_drain_wait(sfull_bar(it % kSSlots), (it / kSSlots) & 1, status);
   }
   tc_fence_before_sync();

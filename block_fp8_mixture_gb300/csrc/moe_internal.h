@@ -30,6 +30,7 @@ constexpr int kBN = 256;
 constexpr int kBK = 128;
 constexpr int kABoxRows = 8;                          // activation rows per TMA box (one swizzle atom)
 constexpr int kGemmThreads = 320;                     // small kernel: TMA, MMA, 8 epilogue warps
+constexpr int kSmallPK = 2;                           // small kernel: K blocks per operand stage
 constexpr int kEpiWarp0 = 2;
 // 128-row-tile kernel: warpgroup 0 = TMA warp, MMA warp, two idle warps (56 registers each after
 // setmaxnreg); warpgroups 1-2 = the 8 promotion/epilogue warps (224 registers each).
