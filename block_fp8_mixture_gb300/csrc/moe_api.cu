@@ -125,6 +125,20 @@ static bool make_map_u8_3d_pk(CUtensorMap* m, const void* base, uint64_t inner, 
 }
 
 // BF16 matrix [rows][cols] stored through 8-row x 64-column boxes with the 128-byte swizzle.
+// The same BF16 matrix as 3-D (column, row inside a 32-row block, 32-row block): boxes of 64
+// columns x 8 rows x 4 blocks store four 8-row groups 32 rows apart (one warp's rows of a tile).
+static bool make_map_bf16_store3(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[3] = {cols, 32, rows / 32};
+  const cuuint64_t strides[2] = {cols * 2, cols * 2 * 32};
+  const cuuint32_t box[3] = {64, 8, 4};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 static bool make_map_bf16_store(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
@@ -367,6 +381,7 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.numerics = a->numerics;
   p.splitk_partial = at<float>(ws, pl.ws.splitk_partial);
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
+  if (!small && p.ksplit != 1) return MOE_ERR_UNSUPPORTED_SHAPE;   // the tile kernels do not split K
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks * p.ksplit;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
   const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
@@ -409,13 +424,14 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.y = static_cast<uint16_t*>(y);
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
-  CUtensorMap tmY;
-  if (!small && !make_map_bf16_store(&tmY, y, pl.H, pl.ws.R_cap))
+  CUtensorMap tmY, tmY3;
+  if (!small && (!make_map_bf16_store(&tmY, y, pl.H, pl.ws.R_cap) ||
+                 !make_map_bf16_store3(&tmY3, y, pl.H, pl.ws.R_cap)))
     return MOE_ERR_CUDA;
   const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
   const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
-                          : bs  ? launch_fc2_bs(tmA, tmB, tmAS, tmS, tmY, p, grid, s)
-                                : launch_fc2(tmA, tmB, tmAS, tmS, tmY, p, grid, s);
+                          : bs  ? launch_fc2_bs(tmA, tmB, tmAS, tmS, tmY, tmY3, p, grid, s)
+                                : launch_fc2(tmA, tmB, tmAS, tmS, tmY, tmY3, p, grid, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

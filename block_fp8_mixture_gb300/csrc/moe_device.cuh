@@ -183,6 +183,16 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int x, int 
       : "memory");
 }
 
+// 3-D tiled bulk tensor store from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int x, int y, int z,
+                                             uint32_t src) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(x), "r"(y), "r"(z), "r"(src)
+      : "memory");
+}
+
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -364,6 +374,13 @@ __device__ __forceinline__ float bf16_bits_to_f32(uint32_t b16) {
 __device__ __forceinline__ uint32_t f32_to_bf16_bits(float v) {
   uint16_t r;
   asm("cvt.rn.bf16.f32 %0, %1;" : "=h"(r) : "f"(v));
+  return r;
+}
+
+// Two fp32 values -> nearest BF16 (ties to even), packed: lo in bits 0..15, hi in bits 16..31.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
   return r;
 }
 

@@ -56,7 +56,8 @@ template <bool kFC1>
 __global__ void __launch_bounds__(kTileThreads, 1)
     k_grouped_gemm(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmAS, const __grid_constant__ CUtensorMap tmS,
-                   const __grid_constant__ CUtensorMap tmY, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tmY,
+                   const __grid_constant__ CUtensorMap tmY3, const GemmParams p) {
   using TC = TileCfg<kFC1>;
   constexpr int kPK = TC::PK;
   constexpr int kStages = TC::Stages;
@@ -88,7 +89,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   static_assert(8 * (kBarT + 5) + 16 <= 1024, "barrier area");
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* mma_consumed = reinterpret_cast<volatile int*>(tmem_slot + 2);
-  volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
   float* red = reinterpret_cast<float*>(ctrl + 1024);   // [2][kBM] row amax of each half
 
   const int warp = threadIdx.x >> 5;
@@ -111,7 +111,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
     *mma_consumed = 0;
-    *last_flag = 0;
     fence_barrier_init();
   }
   if (warp == 0 && lane == 0) {
@@ -302,10 +301,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       if (!ok) break;
 
       if (kFC1) {
-        if (!fc1_item_epilogue(p, w, acc, row, wg, ew, lane, rlive, red, last_flag)) continue;
+        fc1_item_epilogue(p, w, acc, row, wg, rlive, red);
       } else {
         fc2_item_epilogue(p, w, acc, row, wg, q, lane, qlive, rlive, ystage + ew * TC::YWarpBytes,
-                          &tmY);
+                          &tmY, &tmY3);
       }
     }
   }
@@ -336,25 +335,25 @@ __global__ void __launch_bounds__(kTileThreads, 1)
 
 template <bool kFC1>
 static cudaError_t launch_gemm(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
-                               const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p,
-                               int grid, cudaStream_t s) {
+                               const CUtensorMap& tmS, const CUtensorMap& tmY, const CUtensorMap& tmY3,
+                               const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm<kFC1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          TileCfg<kFC1>::Smem);
   if (err != cudaSuccess) return err;
   return launch_pdl(k_grouped_gemm<kFC1>, dim3(grid), dim3(kTileThreads), TileCfg<kFC1>::Smem, s, tmA,
-                    tmB, tmAS, tmS, tmY, p);
+                    tmB, tmAS, tmS, tmY, tmY3, p);
 }
 
 cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
                        const CUtensorMap& tmS, const GemmParams& p, int grid, cudaStream_t s) {
-  return launch_gemm<true>(tmA, tmB, tmAS, tmS, tmA, p, grid, s);   // FC1 stores no BF16 tile
+  return launch_gemm<true>(tmA, tmB, tmAS, tmS, tmA, tmA, p, grid, s);   // FC1 stores no BF16 tile
 }
 
 cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
-                       const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p, int grid,
-                       cudaStream_t s) {
-  return launch_gemm<false>(tmA, tmB, tmAS, tmS, tmY, p, grid, s);
+                       const CUtensorMap& tmS, const CUtensorMap& tmY, const CUtensorMap& tmY3,
+                       const GemmParams& p, int grid, cudaStream_t s) {
+  return launch_gemm<false>(tmA, tmB, tmAS, tmS, tmY, tmY3, p, grid, s);
 }
 
 }  // namespace moe

@@ -207,18 +207,19 @@ cudaError_t launch_batch_prep(const BatchPrepParams& p, cudaStream_t s);
 cudaError_t launch_quant_rows(const QuantRowsParams& p, cudaStream_t s);
 cudaError_t launch_quant(const QuantParams& p, cudaStream_t s);
 // tile kernel maps: tmA activation rows (5-D), tmB weight rows, tmAS activation scales (2-D),
-// tmS weight block scales (1-D, 32-byte boxes), tmY the BF16 output (FC2)
+// tmS weight block scales (1-D, 32-byte boxes), tmY / tmY3 the BF16 output (FC2; 8-row boxes and
+// boxes of four 8-row groups 32 rows apart)
 cudaError_t launch_fc1(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
                        const CUtensorMap& tmS, const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc2(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
-                       const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p, int grid,
-                       cudaStream_t s);
+                       const CUtensorMap& tmS, const CUtensorMap& tmY, const CUtensorMap& tmY3,
+                       const GemmParams& p, int grid, cudaStream_t s);
 // the same tile GEMMs for UE8M0 activation and weight scales, on the block-scaled MMA
 cudaError_t launch_fc1_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
                           const CUtensorMap& tmS, const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc2_bs(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmAS,
-                          const CUtensorMap& tmS, const CUtensorMap& tmY, const GemmParams& p,
-                          int grid, cudaStream_t s);
+                          const CUtensorMap& tmS, const CUtensorMap& tmY, const CUtensorMap& tmY3,
+                          const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc1_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                              const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_fc2_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,

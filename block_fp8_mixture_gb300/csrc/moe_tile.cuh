@@ -78,60 +78,12 @@ __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* s
 // 256 threads.
 constexpr int kTileEpiThreadsBar = 256;
 
-// FC1: acc[0..63] gate sums, acc[64..127] up sums of the thread's row.  With K split across CTAs
-// the split publishes its partial rows and only the last split to arrive continues (returns
-// false for the others).  Then SwiGLU on the BF16-rounded sums and 1x128 requantization of the
-// row's 128 outputs, written to the FC2 input codes and scales.
-__device__ __forceinline__ bool fc1_item_epilogue(const GemmParams& p, const Item& w, float* acc,
-                                                  int row, int wg, int ew, int lane, bool rlive,
-                                                  float* red, volatile int* last_flag) {
+// FC1: acc[0..63] gate sums, acc[64..127] up sums of the thread's row (the tile kernels do not
+// split K).  SwiGLU on the BF16-rounded sums and 1x128 requantization of the row's 128 outputs,
+// written to the FC2 input codes and scales.
+__device__ __forceinline__ void fc1_item_epilogue(const GemmParams& p, const Item& w, float* acc,
+                                                  int row, int wg, bool rlive, float* red) {
   const int I = p.out_cols;
-  if (p.ksplit > 1) {
-    // split-K fix-up: publish this split's partial rows, the last split sums all of them
-    const int pair = rlive ? p.sorted_pair[w.m0 + row] : 0;
-    if (rlive) {
-      float* dst = p.splitk_partial + ((size_t)w.ks * p.P_cap + pair) * (2 * I);
-#pragma unroll
-      for (int i = 0; i < 64; i += 4) {
-        *reinterpret_cast<float4*>(dst + w.nb * kGroup + wg * 64 + i) =
-            make_float4(acc[i], acc[i + 1], acc[i + 2], acc[i + 3]);
-        *reinterpret_cast<float4*>(dst + I + w.nb * kGroup + wg * 64 + i) =
-            make_float4(acc[64 + i], acc[65 + i], acc[66 + i], acc[67 + i]);
-      }
-    }
-    __threadfence();
-    named_barrier_sync(1, kTileEpiThreadsBar);
-    if (ew == 0 && lane == 0) {
-      const int prev = atomicAdd(&p.splitk_count[w.tile * p.n_blocks + w.nb], 1);
-      *last_flag = (prev == p.ksplit - 1);
-    }
-    named_barrier_sync(1, kTileEpiThreadsBar);
-    const bool last = *last_flag != 0;
-    named_barrier_sync(1, kTileEpiThreadsBar);
-    if (!last) return false;
-    __threadfence();
-    if (ew == 0 && lane == 0) p.splitk_count[w.tile * p.n_blocks + w.nb] = 0;
-    if (rlive) {
-#pragma unroll
-      for (int i = 0; i < 128; ++i) acc[i] = 0.0f;
-      for (int s = 0; s < p.ksplit; ++s) {
-        const float* src = p.splitk_partial + ((size_t)s * p.P_cap + pair) * (2 * I);
-#pragma unroll
-        for (int i = 0; i < 64; i += 4) {
-          const float4 g = __ldcg(reinterpret_cast<const float4*>(src + w.nb * kGroup + wg * 64 + i));
-          const float4 u = __ldcg(reinterpret_cast<const float4*>(src + I + w.nb * kGroup + wg * 64 + i));
-          acc[i] = __fadd_rn(acc[i], g.x);
-          acc[i + 1] = __fadd_rn(acc[i + 1], g.y);
-          acc[i + 2] = __fadd_rn(acc[i + 2], g.z);
-          acc[i + 3] = __fadd_rn(acc[i + 3], g.w);
-          acc[64 + i] = __fadd_rn(acc[64 + i], u.x);
-          acc[65 + i] = __fadd_rn(acc[65 + i], u.y);
-          acc[66 + i] = __fadd_rn(acc[66 + i], u.z);
-          acc[67 + i] = __fadd_rn(acc[67 + i], u.w);
-        }
-      }
-    }
-  }
   // SwiGLU on the BF16-rounded FC1 outputs, then 1x128 requantization over the row's 128
   // (gate, up) columns held by this thread (64) and its partner in the other half (64).
   float amax = 0.0f;
@@ -166,19 +118,20 @@ __device__ __forceinline__ bool fc1_item_epilogue(const GemmParams& p, const Ite
     if (wg == 0)
       store_scale(p.a2_s, (size_t)w.nb * p.R_cap + w.m0 + row, s, p.act_fmt == MOE_SCALE_UE8M0);
   }
-  return true;
 }
 
 // FC2: acc[0..127] = the thread's 128 output sums.  BF16 tile out through TMA stores: this warp's
 // rows come in four 8-row groups (rows 32*g + 8*q .. +7).  The warp writes its 32 x 128 block into
-// its own 8 KB staging buffer `buf` (1024-byte aligned) as 128-byte-swizzled 8 x 64 boxes and lane
-// 0 issues the box stores without waiting for them; the buffer is reused one item later, after the
-// stores have read it.  Groups that are only partly live (the end of an expert's rows) are written
-// row by row instead.
+// its own 8 KB staging buffer `buf` (1024-byte aligned) as 128-byte-swizzled 8 x 64 boxes laid out
+// [64-column half][group][row], and lane 0 issues the stores without waiting for them; the buffer
+// is reused one item later, after the stores have read it.  When all four groups are live, one
+// 3-D store (tmY3: 64 columns x 8 rows x 4 groups 32 rows apart) writes each half; otherwise each
+// fully live group is stored on its own (tmY: 64 x 8) and partly live groups are written row by
+// row from registers.
 __device__ __forceinline__ void fc2_item_epilogue(const GemmParams& p, const Item& w,
                                                   const float* acc, int row, int wg, int q,
                                                   int lane, bool qlive, bool rlive, uint8_t* buf,
-                                                  const CUtensorMap* tmY) {
+                                                  const CUtensorMap* tmY, const CUtensorMap* tmY3) {
   const int col0 = w.nb * kBN + wg * kGroup;
   if (!qlive || col0 >= p.out_cols) return;
   const uint32_t buf_s = smem_addr(buf);
@@ -190,34 +143,36 @@ __device__ __forceinline__ void fc2_item_epilogue(const GemmParams& p, const Ite
   if (grow_mine + 8 <= w.live) {
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      uint32_t wd[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        wd[j] = f32_to_bf16_bits(acc[c * 8 + 2 * j]) | (f32_to_bf16_bits(acc[c * 8 + 2 * j + 1]) << 16);
-      const int box = c >> 3, cc = c & 7;
-      *reinterpret_cast<uint4*>(buf + g_mine * 2048 + box * 1024 + t * 128 + ((cc ^ t) << 4)) =
-          make_uint4(wd[0], wd[1], wd[2], wd[3]);
+      const float* v = acc + c * 8;
+      const int half = c >> 3, cc = c & 7;
+      *reinterpret_cast<uint4*>(buf + half * 4096 + g_mine * 1024 + t * 128 + ((cc ^ t) << 4)) =
+          make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
     }
   } else if (rlive) {
     uint16_t* dst = p.y + (size_t)(w.m0 + row) * p.out_cols + col0;
 #pragma unroll
-    for (int v = 0; v < 16; ++v) {
-      uint32_t wd[4];
-#pragma unroll
-      for (int j = 0; j < 4; ++j)
-        wd[j] = f32_to_bf16_bits(acc[v * 8 + 2 * j]) | (f32_to_bf16_bits(acc[v * 8 + 2 * j + 1]) << 16);
-      *reinterpret_cast<uint4*>(dst + v * 8) = make_uint4(wd[0], wd[1], wd[2], wd[3]);
+    for (int c = 0; c < 16; ++c) {
+      const float* v = acc + c * 8;
+      *reinterpret_cast<uint4*>(dst + c * 8) =
+          make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
     }
   }
   fence_proxy_async_smem();
   __syncwarp();
   if (lane == 0) {
+    if (96 + 8 * q + 8 <= w.live) {
+      tma_store_3d(tmY3, col0, 8 * q, w.m0 / 32, buf_s);
+      tma_store_3d(tmY3, col0 + 64, 8 * q, w.m0 / 32, buf_s + 4096);
+    } else {
 #pragma unroll
-    for (int g = 0; g < 4; ++g) {
-      const int grow = 32 * g + 8 * q;
-      if (grow + 8 <= w.live) {
-        tma_store_2d(tmY, col0, w.m0 + grow, buf_s + g * 2048);
-        tma_store_2d(tmY, col0 + 64, w.m0 + grow, buf_s + g * 2048 + 1024);
+      for (int g = 0; g < 4; ++g) {
+        const int grow = 32 * g + 8 * q;
+        if (grow + 8 <= w.live) {
+          tma_store_2d(tmY, col0, w.m0 + grow, buf_s + g * 1024);
+          tma_store_2d(tmY, col0 + 64, w.m0 + grow, buf_s + 4096 + g * 1024);
+        }
       }
     }
     bulk_commit_group();
