@@ -42,8 +42,8 @@ class MoeError(RuntimeError):
 class WsPlan(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in (
         "status", "num_tiles", "seg_start", "live_end", "sorted_pair", "pair_row", "tile_expert",
-        "num_chunks", "chunk_row0", "align_hist", "a1_q", "a1_s", "a2_q", "a2_s", "y", "splitk_partial",
-        "splitk_count", "total_bytes")] + [
+        "num_chunks", "chunk_row0", "align_hist", "a1_q", "a1_s", "a2_q", "a2_s", "y", "g1",
+        "splitk_partial", "splitk_count", "total_bytes")] + [
         ("R_cap", ctypes.c_int32), ("T_cap", ctypes.c_int32), ("C_cap", ctypes.c_int32),
         ("P_cap", ctypes.c_int32), ("fc1_ksplit", ctypes.c_int32), ("small_batch", ctypes.c_int32),
         ("align_ctas", ctypes.c_int32)]
@@ -181,6 +181,7 @@ def workspace_views(ws, M_cap: int, E: int, H: int, I: int, topk: int, act_fmt: 
         "a2_q": view(p["a2_q"], R * I, torch.uint8, 1).view(R, I),
         "a2_s": view(p["a2_s"], (I // 128) * R, sdt, ssz).view(I // 128, R),
         "y": view(p["y"], R * H, torch.int16, 2).view(R, H),
+        "g1": view(p["g1"], R * 2 * I, torch.int16, 2).view(R, 2 * I) if p["g1"] else None,
     }
 
 

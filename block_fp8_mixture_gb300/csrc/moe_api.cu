@@ -77,6 +77,9 @@ moe_status make_plan(int M_cap, int E, int H, int I, int topk, int act_fmt, Plan
   w.a2_q = take((size_t)R_cap * I);
   w.a2_s = take((size_t)(I / kGroup) * R_cap * sc);
   w.y = take((size_t)R_cap * H * 2);
+  // the tile schedule with fp32 activation scales runs SwiGLU + requantization as its own kernel
+  // on the BF16 FC1 outputs (UE8M0 layers keep it in the block-scaled GEMM's overlapped epilogue)
+  w.g1 = (!w.small_batch && act_fmt != MOE_SCALE_UE8M0) ? take((size_t)R_cap * 2 * I * 2) : 0;
   w.splitk_partial = take(w.fc1_ksplit > 1 ? (size_t)w.fc1_ksplit * P_cap * 2 * I * 4 : 0);
   w.splitk_count = take(w.fc1_ksplit > 1 ? (size_t)w.C_cap * (I / kGroup) * 4 : 0);
   w.total_bytes = off;
@@ -385,9 +388,29 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks * p.ksplit;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
   const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
-  const cudaError_t err = small ? launch_fc1_small(tmA, tmB, tmS, p, grid, s)
-                          : bs  ? launch_fc1_bs(tmA, tmB, tmAS, tmS, p, grid, s)
-                                : launch_fc1(tmA, tmB, tmAS, tmS, p, grid, s);
+  // tile schedule with fp32 activation scales: BF16 FC1 outputs, then SwiGLU + requant kernel
+  const bool split_epilogue = !small && !bs && pl.ws.g1 != 0;
+  if (split_epilogue) p.g1 = at<uint16_t>(ws, pl.ws.g1);
+  cudaError_t err = small ? launch_fc1_small(tmA, tmB, tmS, p, grid, s)
+                    : bs  ? launch_fc1_bs(tmA, tmB, tmAS, tmS, p, grid, s)
+                          : launch_fc1(tmA, tmB, tmAS, tmS, p, grid, s);
+  if (err == cudaSuccess && split_epilogue) {
+    SwigluQuantParams q;
+    q.g1 = p.g1;
+    q.R_cap = pl.ws.R_cap;
+    q.I = pl.I;
+    q.num_tiles = p.num_tiles;
+    q.tile_expert = p.tile_expert;
+    q.live_end = p.live_end;
+    q.all_tiles = tile_row0 != nullptr ? 1 : 0;
+    q.clamp_mode = a->clamp_mode;
+    q.clamp_limit = a->clamp_limit;
+    q.numerics = a->numerics;
+    q.fmt = pl.act_fmt;
+    q.a2_q = p.a2_q;
+    q.a2_s = p.a2_s;
+    err = launch_swiglu_quant(q, s);
+  }
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -489,6 +512,7 @@ static moe_status make_batched_plan(int E, int max_m, int H, int I, int act_fmt,
   w.a1_s = take((size_t)(H / kGroup) * R * sc);
   w.a2_q = take((size_t)R * I);
   w.a2_s = take((size_t)(I / kGroup) * R * sc);
+  w.g1 = (!w.small_batch && act_fmt != MOE_SCALE_UE8M0) ? take((size_t)R * 2 * I * 2) : 0;
   w.total_bytes = off;
   plan->M_cap = max_m;
   plan->E = E;

@@ -388,6 +388,21 @@ __device__ __forceinline__ float bf16_round(float v) {
   return bf16_bits_to_f32(f32_to_bf16_bits(v));
 }
 
+// SiLU(g) * u with the optional clamp, fp32, IEEE division, no fused multiply-add.
+__device__ __forceinline__ float swiglu(float g, float u, int mode, float lim) {
+  if (mode == MOE_CLAMP_BEFORE_SILU) {
+    g = fminf(g, lim);
+    u = fminf(fmaxf(u, -lim), lim);
+  }
+  const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-g)));   // correctly rounded 1/(1+e^-g)
+  float silu = __fmul_rn(g, sig);
+  if (mode == MOE_CLAMP_AFTER_SILU) {
+    silu = fminf(silu, lim);
+    u = fminf(fmaxf(u, -lim), lim);
+  }
+  return __fmul_rn(silu, u);
+}
+
 // 1x128 group scale: max(RN(amax/448), RN(1/(448*512))); POW2/UE8M0 round up to a power of two.
 __device__ __forceinline__ float group_scale(float amax, int fmt) {
   float s = fmaxf(__fdiv_rn(amax, 448.0f), kScaleFloor);

@@ -301,7 +301,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       if (!ok) break;
 
       if (kFC1) {
-        fc1_item_epilogue(p, w, acc, row, wg, rlive, red);
+        if (p.g1 != nullptr)
+          fc1_item_store_g1(p, w, acc, row, wg, rlive);
+        else
+          fc1_item_epilogue(p, w, acc, row, wg, rlive, red);
       } else {
         fc2_item_epilogue(p, w, acc, row, wg, q, lane, qlive, rlive, ystage + ew * TC::YWarpBytes,
                           &tmY, &tmY3);

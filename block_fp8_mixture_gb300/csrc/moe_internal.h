@@ -172,6 +172,25 @@ struct GemmParams {
   // FC2 epilogue
   uint16_t* y;
   int32_t* status;
+  // tile schedule, fp32 activation scales: FC1 writes BF16 (gate | up) rows here instead of
+  // running SwiGLU + requantization in its epilogue (nullptr: fused epilogue)
+  uint16_t* g1;
+};
+
+// SwiGLU + 1x128 requantization of the BF16 FC1 outputs of live workspace rows.
+struct SwigluQuantParams {
+  const uint16_t* g1;       // [R_cap][2I]
+  int R_cap, I;
+  const int32_t* num_tiles;
+  const int32_t* tile_expert;
+  const int32_t* live_end;
+  int all_tiles;            // 1: tile_expert holds every tile (batched layout), 0: tiles < num_tiles
+  int clamp_mode;
+  float clamp_limit;
+  int numerics;
+  int fmt;
+  uint8_t* a2_q;
+  void* a2_s;
 };
 
 struct ReduceParams {
@@ -225,5 +244,6 @@ cudaError_t launch_fc1_small(const CUtensorMap& tmA, const CUtensorMap& tmB, con
 cudaError_t launch_fc2_small(const CUtensorMap& tmA, const CUtensorMap& tmB, const CUtensorMap& tmS,
                              const GemmParams& p, int grid, cudaStream_t s);
 cudaError_t launch_reduce(const ReduceParams& p, cudaStream_t s);
+cudaError_t launch_swiglu_quant(const SwigluQuantParams& p, cudaStream_t s);
 
 }  // namespace moe

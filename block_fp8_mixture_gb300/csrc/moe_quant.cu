@@ -168,3 +168,62 @@ cudaError_t launch_quant_rows(const QuantRowsParams& p, cudaStream_t s) {
 }
 
 }  // namespace moe
+
+namespace moe {
+
+// SwiGLU + 1x128 requantization as its own kernel (vLLM "per-layer activation scale format + fused
+// SiLU+quant", Details: the fused silu_and_mul_per_block_quant kernel reads the FP32/BF16 gate and
+// up halves and writes FP8 codes with 1x128 scales).  The tile schedule with fp32 activation scales
+// uses it on the BF16 FC1 outputs; the arithmetic is that of the fused FC1 epilogue.  One half-warp
+// per (row, 128-column group): 16-byte loads of 8 gate and 8 up values per lane, shuffle amax.
+__global__ void __launch_bounds__(kQuantThreads) k_swiglu_quant(SwigluQuantParams p) {
+  const int groups = p.I / kGroup;
+  const int half = (threadIdx.x >> 4) & 1;
+  const int l16 = threadIdx.x & 15;
+  const uint32_t hmask = 0xFFFFu << (16 * half);
+  const long gid = (long)blockIdx.x * kGroupsPerBlock + (threadIdx.x >> 4);
+  const long row = gid / groups;
+  const int g = (int)(gid % groups);
+  grid_dep_wait();
+  grid_dep_launch_dependents();
+  if (row >= p.R_cap) return;                 // the whole half-warp leaves together
+  const int t = (int)(row / kBM);
+  if (!p.all_tiles && t >= *p.num_tiles) return;
+  if (row >= p.live_end[p.tile_expert[t]]) return;
+
+  const uint16_t* src = p.g1 + row * (2 * p.I) + g * kGroup + l16 * 8;
+  const uint4 gr = *reinterpret_cast<const uint4*>(src);
+  const uint4 ur = *reinterpret_cast<const uint4*>(src + p.I);
+  const uint32_t gw[4] = {gr.x, gr.y, gr.z, gr.w};
+  const uint32_t uw[4] = {ur.x, ur.y, ur.z, ur.w};
+  float h[8];
+  float amax = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const uint32_t gb = (i & 1) ? gw[i >> 1] >> 16 : gw[i >> 1] & 0xFFFFu;
+    const uint32_t ub = (i & 1) ? uw[i >> 1] >> 16 : uw[i >> 1] & 0xFFFFu;
+    float v = swiglu(bf16_bits_to_f32(gb), bf16_bits_to_f32(ub), p.clamp_mode, p.clamp_limit);
+    if (p.numerics == MOE_NUMERICS_RECIPROCAL) v = bf16_round(v);
+    h[i] = v;
+    amax = fmaxf(amax, fabsf(v));
+  }
+#pragma unroll
+  for (int d = 8; d >= 1; d >>= 1) amax = fmaxf(amax, __shfl_xor_sync(hmask, amax, d));
+  float inv;
+  const float s = group_scale_numerics(amax, p.fmt, p.numerics, &inv);
+  const uint32_t q0 = cvt_e4m3x2(quant_div(h[0], s, inv), quant_div(h[1], s, inv)) |
+                      (cvt_e4m3x2(quant_div(h[2], s, inv), quant_div(h[3], s, inv)) << 16);
+  const uint32_t q1 = cvt_e4m3x2(quant_div(h[4], s, inv), quant_div(h[5], s, inv)) |
+                      (cvt_e4m3x2(quant_div(h[6], s, inv), quant_div(h[7], s, inv)) << 16);
+  *reinterpret_cast<uint2*>(p.a2_q + (size_t)row * p.I + g * kGroup + l16 * 8) = make_uint2(q0, q1);
+  if (l16 == 0) store_scale(p.a2_s, (size_t)g * p.R_cap + row, s, p.fmt == MOE_SCALE_UE8M0);
+}
+
+cudaError_t launch_swiglu_quant(const SwigluQuantParams& p, cudaStream_t s) {
+  const long groups = (long)p.R_cap * (p.I / kGroup);
+  const long blocks = (groups + kGroupsPerBlock - 1) / kGroupsPerBlock;
+  if (blocks == 0) return cudaSuccess;
+  return launch_pdl(k_swiglu_quant, dim3((unsigned)blocks), dim3(kQuantThreads), 0, s, p);
+}
+
+}  // namespace moe

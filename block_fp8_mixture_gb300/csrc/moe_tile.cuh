@@ -46,21 +46,6 @@ __device__ __forceinline__ void scale_rows(const GemmParams& p, const Item& w, i
   }
 }
 
-// SiLU(g) * u with the optional clamp, fp32, IEEE division, no fused multiply-add.
-__device__ __forceinline__ float swiglu(float g, float u, int mode, float lim) {
-  if (mode == MOE_CLAMP_BEFORE_SILU) {
-    g = fminf(g, lim);
-    u = fminf(fmaxf(u, -lim), lim);
-  }
-  const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-g)));   // correctly rounded 1/(1+e^-g)
-  float silu = __fmul_rn(g, sig);
-  if (mode == MOE_CLAMP_AFTER_SILU) {
-    silu = fminf(silu, lim);
-    u = fminf(fmaxf(u, -lim), lim);
-  }
-  return __fmul_rn(silu, u);
-}
-
 // Bounded wait used while tearing down: ignores the abort flag.
 __device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, int* status) {
   const uint64_t t0 = global_timer_ns();
@@ -117,6 +102,27 @@ __device__ __forceinline__ void fc1_item_epilogue(const GemmParams& p, const Ite
     }
     if (wg == 0)
       store_scale(p.a2_s, (size_t)w.nb * p.R_cap + w.m0 + row, s, p.act_fmt == MOE_SCALE_UE8M0);
+  }
+}
+
+// FC1 of the tile schedule with fp32 activation scales: the row's 64 gate and 64 up sums, rounded
+// to BF16, go to the FC1 output rows (gate | up); SwiGLU and the requantization run in their own
+// kernel.  Only live rows are written.
+__device__ __forceinline__ void fc1_item_store_g1(const GemmParams& p, const Item& w,
+                                                  const float* acc, int row, int wg, bool rlive) {
+  if (!rlive) return;
+  const int I = p.out_cols;
+  uint16_t* g = p.g1 + (size_t)(w.m0 + row) * (2 * I) + w.nb * kGroup + wg * 64;
+#pragma unroll
+  for (int half = 0; half < 2; ++half) {
+    uint16_t* dst = g + half * I;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const float* v = acc + half * 64 + c * 8;
+      *reinterpret_cast<uint4*>(dst + c * 8) =
+          make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
+    }
   }
 }
 

@@ -93,11 +93,14 @@ typedef enum { MOE_NUMERICS_DIVIDE = 0, MOE_NUMERICS_RECIPROCAL = 1 } moe_numeri
  *   a2_q         uint8[R_cap][I]       FC2 input, E4M3 codes
  *   a2_s         [I/128][R_cap]        FC2 input scales, column-major (fp32 or uint8)
  *   y            bf16[R_cap][H]        FC2 output per pair row (routing weights not applied)
+ *   g1           bf16[R_cap][2I]       FC1 outputs (gate | up) of the 128-row-tile schedule with
+ *                                      fp32 activation scales, where SwiGLU + requantization run as
+ *                                      their own kernel; 0 when the plan has none
  *   splitk       fp32 partial sums and int32 tile counters of the split-K FC1 schedule */
 typedef struct {
   size_t status, num_tiles, seg_start, live_end, sorted_pair, pair_row, tile_expert;
   size_t num_chunks, chunk_row0, align_hist;
-  size_t a1_q, a1_s, a2_q, a2_s, y, splitk_partial, splitk_count;
+  size_t a1_q, a1_s, a2_q, a2_s, y, g1, splitk_partial, splitk_count;
   size_t total_bytes;
   int32_t R_cap;   /* workspace rows: roundup(P_cap + min(E, P_cap) * 127, 128) */
   int32_t T_cap;   /* R_cap / 128 */

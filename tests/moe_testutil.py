@@ -116,3 +116,5 @@ def check_untouched(case, views):
     for name in ("a1_q", "a2_q"):
         assert bool((views[name].index_select(0, idx) == 0xFF).all()), f"{name} padding written"
     assert bool((views["y"].index_select(0, idx) == -1).all()), "y padding written"
+    if views.get("g1") is not None:
+        assert bool((views["g1"].index_select(0, idx) == -1).all()), "FC1 output padding written"
