@@ -1,5 +1,6 @@
-// Persistent grouped FP8 x FP8 GEMM over live row tiles, with the FC1 (SwiGLU + 1x128 requant)
-// and FC2 (BF16 store) epilogues.
+// Persistent grouped FP8 x FP8 GEMM over live 128-row tiles for FP32 block scales (per-128-K
+// promotion through registers), with the FC1 (SwiGLU + 1x128 requant, or BF16 (gate | up) rows for
+// the separate SwiGLU kernel) and FC2 (BF16 store) epilogues.
 //
 // (vLLM "Skip padded work in block-FP8 DeepGemmExperts", Purpose: both grouped GEMMs visit only
 // the live (expert, row-tile) work named by the prefix-sum endpoints, and the fused activation
@@ -8,8 +9,8 @@
 // decode-sized batches on Hopper", human review: per 128-wide K block the partial sum is scaled by
 // the product a_scale*b_scale formed first.)
 //
-// Work item = (live row tile, output column block, K split).  One CTA per SM walks items
-// blockIdx.x, blockIdx.x + gridDim.x, ...; inside the CTA:
+// Work item = (live row tile, output column block).  One CTA per SM walks items blockIdx.x,
+// blockIdx.x + gridDim.x, ...; inside the CTA:
 //   warp 0 (one lane)  TMA producer.  Each stage of the operand ring receives the tile's 128
 //                      activation rows (one 5-D box that also permutes the 8-row groups, below)
 //                      and its 256 weight rows (one box, 128-byte swizzle) for one or two 128-wide
@@ -19,20 +20,22 @@
 //                      completion, the promotion warps release the scale slot once they have
 //                      read it.  Rows of a tile past the expert's live end are loaded too (they
 //                      stay inside the workspace) and their results are discarded.
-//   warp 1 (one lane)  MMA issuer: 4 x tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32) per K block
-//                      into one of two 256-column fp32 accumulators in tensor memory.
-//   warps 2..9         promotion + epilogue.  A thread owns one row and 128 of the 256 columns;
-//                      per K block it reads its partial sums from tensor memory and accumulates
+//   warp 1 (one lane)  MMA issuer: 4 x 2 tcgen05.mma kind::f8f6f4 (M=128, N=128, K=32) per K
+//                      block into one of two 256-column fp32 accumulators in tensor memory.
+//   warps 4..11        promotion + epilogue (224 registers after setmaxnreg).  A thread owns one
+//                      row and 128 of the 256 columns; per K block it reads its partial sums from
+//                      tensor memory (two loads in flight per wait) and accumulates
 //                      acc = fma(partial, a_scale*b_scale, acc) in registers, then releases the
 //                      accumulator so the MMA of a later K block overlaps the promotion.
 // Row placement: 8-row group j = 4a + b of the tile (rows 32a + 8b ..) lands in shared-memory group
 // 4b + a, i.e. tensor-memory lanes 32b + 8a .. +7, so even a tile with 8..32 live rows keeps all
 // four lane quarters (all eight promotion warps) busy.
 // FC1 columns: 128 gate rows of W13 and the matching 128 up rows, so a thread owns 64 (gate, up)
-// pairs of one row; the SwiGLU and the 1x128 requantization need only the row amax of the two
-// threads sharing the row.  FC2 columns: 256 consecutive hidden columns, BF16 out.
-// Small batches split K across CTAs (FC1 only): each split writes its fp32 partial rows, the last
-// split to arrive (atomic counter per item) sums the splits in fixed order and runs the epilogue.
+// pairs of one row.  When the workspace has an FC1 output region the thread stores its BF16 gate
+// and up values and SwiGLU + requantization run as their own kernel (the fused epilogue cannot
+// overlap the mainloop); otherwise it applies SwiGLU and the 1x128 requantization, which need only
+// the row amax of the two threads sharing the row.  FC2 columns: 256 consecutive hidden columns,
+// BF16 out.
 #include "moe_tile.cuh"
 
 namespace moe {
