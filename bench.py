@@ -228,9 +228,12 @@ def run_ours(args, rank, world):
     dev_w = tuple(torch.from_numpy(a).cuda() for a in (weights.w13, weights.s13, weights.w2, weights.s2))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
-    do_sweep = args.workload == WORKLOAD and not (args.no_sweep or args.profile_run)
-    sweep = sorted(set(SWEEP_M) | {args.M}) if do_sweep else [args.M]
-    benches = {M: LayerBench(args.workload, M, args.n if M == args.M else M, rank, weights, dev_w)
+    do_sweep = (args.workload == WORKLOAD or args.sweep) and not (args.no_sweep or args.profile_run)
+    sweep_points = SWEEP_M if args.workload == WORKLOAD else [m for m, _ in synth.SWEEPS[args.workload]]
+    sweep = sorted(set(sweep_points) | {args.M}) if do_sweep else [args.M]
+    live = dict(synth.SWEEPS[args.workload])
+    benches = {M: LayerBench(args.workload, M, args.n if M == args.M else live.get(M, M), rank,
+                             weights, dev_w)
                for M in sweep}
 
     # graphs of the whole forward, one per M
@@ -471,6 +474,8 @@ def main():
     ap.add_argument("--M", type=int, default=None, help="token capacity of the headline point")
     ap.add_argument("--n", type=int, default=None, help="live tokens (default: M)")
     ap.add_argument("--no-sweep", action="store_true")
+    ap.add_argument("--sweep", action="store_true",
+                    help="also measure every M of the workload's sweep (the decode workload always does)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-run", action="store_true",
                     help="only W + K graph replays of the headline point (for ncu captures)")
