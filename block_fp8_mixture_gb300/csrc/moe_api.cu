@@ -355,7 +355,8 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
   const bool small = pl.ws.small_batch != 0;
   const uint64_t n_ws = (uint64_t)pl.E * (2 * pl.I / kGroup) * (pl.H / kGroup);
-  constexpr uint32_t pk = TileCfg<true>::PK;
+  const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
+  const uint32_t pk = bs ? TileCfg<true, true>::PK : TileCfg<true>::PK;
   const bool maps_ok =
       small ? make_map_tok_chunk(&tmA, at<void>(ws, pl.ws.a1_q), pl.H, pl.ws.R_cap, kSmallPK) &&
                   make_map_w13_tile(&tmB, a->w13, pl.H, (uint64_t)pl.E * 2 * pl.I, pl.I, kSmallPK) &&
@@ -387,7 +388,6 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   if (!small && p.ksplit != 1) return MOE_ERR_UNSUPPORTED_SHAPE;   // the tile kernels do not split K
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks * p.ksplit;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
-  const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
   // tile schedule with fp32 activation scales: BF16 FC1 outputs, then SwiGLU + requant kernel
   const bool split_epilogue = !small && !bs && pl.ws.g1 != 0;
   if (split_epilogue) p.g1 = at<uint16_t>(ws, pl.ws.g1);

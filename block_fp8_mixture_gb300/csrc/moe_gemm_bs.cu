@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
                       const __grid_constant__ CUtensorMap tmAS, const __grid_constant__ CUtensorMap tmS,
                       const __grid_constant__ CUtensorMap tmY,
                       const __grid_constant__ CUtensorMap tmY3, const GemmParams p) {
-  using TC = TileCfg<kFC1>;
+  using TC = TileCfg<kFC1, true>;
   constexpr int kPK = TC::PK;
   constexpr int kStages = TC::Stages;
   constexpr int kStageBytes = TC::StageBytes;
@@ -355,9 +355,9 @@ static cudaError_t launch_gemm_bs(const CUtensorMap& tmA, const CUtensorMap& tmB
                                   const GemmParams& p, int grid, cudaStream_t s) {
   cudaError_t err = cudaFuncSetAttribute(k_grouped_gemm_bs<kFC1>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         TileCfg<kFC1>::Smem);
+                                         TileCfg<kFC1, true>::Smem);
   if (err != cudaSuccess) return err;
-  return launch_pdl(k_grouped_gemm_bs<kFC1>, dim3(grid), dim3(kBsThreads), TileCfg<kFC1>::Smem, s,
+  return launch_pdl(k_grouped_gemm_bs<kFC1>, dim3(grid), dim3(kBsThreads), TileCfg<kFC1, true>::Smem, s,
                     tmA, tmB, tmAS, tmS, tmY, tmY3, p);
 }
 
