@@ -51,6 +51,16 @@ def test_layer_largest_k_split(act_fmt, weight_fmt):
     _layer_check(case)
 
 
+@pytest.mark.parametrize("M,n", [(4, 4), (24, 19), (64, 64)])
+def test_layer_decode_shaped(M, n):
+    """Decode-shaped layers (K = 32 blocks, 64 experts) at batch sizes whose (chunk, column block)
+    units leave the SMs partly idle, fill them, or give a ragged last round."""
+    shape = synth.small_shape("dec_shape", E=64, H=4096, I=512, topk=8, clamp_mode=1, limit=7.0)
+    case = synth.make_case("dec_shape", M, n, shape=shape)
+    assert _plan(case)["small_batch"] == 1
+    _layer_check(case)
+
+
 def test_layer_ue8m0_tile_k1():
     """Block-scaled MMA path with a single K block per GEMM."""
     shape = synth.small_shape("bs_k1", E=2, H=128, I=128, topk=2, act_fmt=2, weight_fmt=2)
