@@ -148,7 +148,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // ------------------------------------------------------------ producer
     int sc = 0;
     bool ok = true;
-    const uint64_t pol_w = policy_evict_first();
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Item w = decode_item(p, item);
       // FC1: 128 gate rows and the matching 128 up rows (the map's outer dimension steps I rows);
@@ -177,9 +176,9 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint32_t sS = slot0 + sl * kScaleSlotBytes;
         tma_load_5d(sA, &tmA, 0, 0, kbs, w.m0 / 32, 0, full_bar(s));
         if (kFC1)
-          tma_load_4d_hint(sB, &tmB, 0, brow0, kbs, 0, full_bar(s), pol_w);
+          tma_load_4d(sB, &tmB, 0, brow0, kbs, 0, full_bar(s));
         else
-          tma_load_3d_hint(sB, &tmB, 0, brow0, kbs, full_bar(s), pol_w);
+          tma_load_3d(sB, &tmB, 0, brow0, kbs, full_bar(s));
         tma_load_2d(sS, &tmAS, w.m0, kbs, sfull_bar(sl));
         // a 32-byte box from the 16-byte boundary at or below the stage's first block scale
         // holds the scales of all kPK K blocks

@@ -133,8 +133,7 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       // ---------------------------------------------------------- producer
       int sc = 0;
       bool ok = true;
-      const uint64_t pol_w = policy_evict_first();
-      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+        for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
         const Item w = decode_item(p, item);
         const int brow0 = kFC1 ? w.e * p.b_rows_per_expert + w.nb * kGroup
                                : w.e * p.b_rows_per_expert + w.nb * kBN;
@@ -157,9 +156,9 @@ __global__ void __launch_bounds__(kBsThreads, 1)
           const uint32_t sS = slot0 + sl * kScaleSlotBytes;
           tma_load_5d(sA, &tmA, 0, 0, kbs, w.m0 / 32, 0, full_bar(s));
           if (kFC1)
-            tma_load_4d_hint(sB, &tmB, 0, brow0, kbs, 0, full_bar(s), pol_w);
+            tma_load_4d(sB, &tmB, 0, brow0, kbs, 0, full_bar(s));
           else
-            tma_load_3d_hint(sB, &tmB, 0, brow0, kbs, full_bar(s), pol_w);
+            tma_load_3d(sB, &tmB, 0, brow0, kbs, full_bar(s));
           tma_load_2d(sS, &tmAS, w.m0, kbs, sfull_bar(sl));
           const int i0 = sr0 * KB + kbs;
           tma_load_1d(sS + kSlotW, &tmS, i0 - i0 % 16, sfull_bar(sl));
