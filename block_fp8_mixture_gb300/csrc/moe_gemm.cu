@@ -148,8 +148,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     // ------------------------------------------------------------ producer
     int sc = 0;
     bool ok = true;
+    const uint64_t pol_once = policy_evict_first();
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Item w = decode_item(p, item);
+      const bool shared = expert_weights_shared(p, w, num_tiles);
       // FC1: 128 gate rows and the matching 128 up rows (the map's outer dimension steps I rows);
       // FC2: 256 consecutive hidden rows (past the expert's last block they are never used)
       const int brow0 = kFC1 ? w.e * p.b_rows_per_expert + w.nb * kGroup
@@ -175,10 +177,14 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint32_t sB = sA + kABytes;
         const uint32_t sS = slot0 + sl * kScaleSlotBytes;
         tma_load_5d(sA, &tmA, 0, 0, kbs, w.m0 / 32, 0, full_bar(s));
-        if (kFC1)
+        if (kFC1 && shared)
           tma_load_4d(sB, &tmB, 0, brow0, kbs, 0, full_bar(s));
-        else
+        else if (kFC1)
+          tma_load_4d_hint(sB, &tmB, 0, brow0, kbs, 0, full_bar(s), pol_once);
+        else if (shared)
           tma_load_3d(sB, &tmB, 0, brow0, kbs, full_bar(s));
+        else
+          tma_load_3d_hint(sB, &tmB, 0, brow0, kbs, full_bar(s), pol_once);
         tma_load_2d(sS, &tmAS, w.m0, kbs, sfull_bar(sl));
         // a 32-byte box from the 16-byte boundary at or below the stage's first block scale
         // holds the scales of all kPK K blocks

@@ -92,6 +92,23 @@ __device__ __forceinline__ void s_drain_wait(uint32_t bar, uint32_t parity, int*
   }
 }
 
+// One trip of a rolled per-token loop over a register array: a[0..n-1] <- a[1..n-1], a[0] for
+// n = 4 or 16 (n trips restore the order; entries past n are untouched).
+__device__ __forceinline__ void rotate_tokens(float* a, int n) {
+  if (n == 4) {
+    const float t = a[0];
+    a[0] = a[1];
+    a[1] = a[2];
+    a[2] = a[3];
+    a[3] = t;
+  } else {
+    const float t = a[0];
+#pragma unroll
+    for (int i = 0; i < 15; ++i) a[i] = a[i + 1];
+    a[15] = t;
+  }
+}
+
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
@@ -345,23 +362,24 @@ __global__ void __launch_bounds__(kSThreads, 1)
 
       if (kFC1) {
         // The epilogue runs once per item, so its code is usually cold in the instruction cache
-        // (and, after other work has passed through L2, in L2 too): the per-token loops stay
-        // rolled, with the token values in a small local array, to keep the fetched code short.
+        // (and, after other work has passed through L2, in L2 too).  Each per-token loop stays
+        // rolled and works on entry 0 of register arrays that rotate by one token per trip:
+        // short code, values in registers.  `trips` (4 when this half holds at most four tokens,
+        // else 16) trips of rotate_tokens restore the order.
         const int I = p.out_cols;
-        float gv[16], uv[16];
-#pragma unroll
-        for (int c = 0; c < 16; ++c) {
-          gv[c] = acc0[c];
-          uv[c] = acc1[c];
-        }
+        const int trips = ntok <= 4 ? 4 : 16;
         if (p.ksplit > 1) {
           // split-K fix-up over pairs: partial[ks][pair][2I], the last split sums in split order
 #pragma unroll 1
-          for (int c = 0; c < ntok; ++c) {
-            const int pair = p.sorted_pair[w.row0 + half * 16 + c];
-            float* dst = p.splitk_partial + ((size_t)w.ks * p.P_cap + pair) * (2 * I);
-            dst[w.nb * kGroup + j] = gv[c];
-            dst[I + w.nb * kGroup + j] = uv[c];
+          for (int c = 0; c < trips; ++c) {
+            if (c < ntok) {
+              const int pair = p.sorted_pair[w.row0 + half * 16 + c];
+              float* dst = p.splitk_partial + ((size_t)w.ks * p.P_cap + pair) * (2 * I);
+              dst[w.nb * kGroup + j] = acc0[0];
+              dst[I + w.nb * kGroup + j] = acc1[0];
+            }
+            rotate_tokens(acc0, trips);
+            rotate_tokens(acc1, trips);
           }
           __threadfence();
           named_barrier_sync(1, 256);
@@ -376,53 +394,65 @@ __global__ void __launch_bounds__(kSThreads, 1)
           __threadfence();
           if (ew == 0 && lane == 0) p.splitk_count[w.chunk * p.n_blocks + w.nb] = 0;
 #pragma unroll 1
-          for (int c = 0; c < ntok; ++c) {
-            const int pair = p.sorted_pair[w.row0 + half * 16 + c];
-            // every split's load first (one round trip), then the sum in split order
-            float ga[kMaxKSplit], ua[kMaxKSplit];
+          for (int c = 0; c < trips; ++c) {
+            if (c < ntok) {
+              const int pair = p.sorted_pair[w.row0 + half * 16 + c];
+              // every split's load first (one round trip), then the sum in split order
+              float ga[kMaxKSplit], ua[kMaxKSplit];
 #pragma unroll
-            for (int s = 0; s < kMaxKSplit; ++s) {
-              if (s < p.ksplit) {
-                const float* src = p.splitk_partial + ((size_t)s * p.P_cap + pair) * (2 * I);
-                ga[s] = __ldcg(src + w.nb * kGroup + j);
-                ua[s] = __ldcg(src + I + w.nb * kGroup + j);
+              for (int s = 0; s < kMaxKSplit; ++s) {
+                if (s < p.ksplit) {
+                  const float* src = p.splitk_partial + ((size_t)s * p.P_cap + pair) * (2 * I);
+                  ga[s] = __ldcg(src + w.nb * kGroup + j);
+                  ua[s] = __ldcg(src + I + w.nb * kGroup + j);
+                }
               }
-            }
-            float g = 0.0f, u = 0.0f;
+              float g = 0.0f, u = 0.0f;
 #pragma unroll
-            for (int s = 0; s < kMaxKSplit; ++s) {
-              if (s < p.ksplit) {
-                g = __fadd_rn(g, ga[s]);
-                u = __fadd_rn(u, ua[s]);
+              for (int s = 0; s < kMaxKSplit; ++s) {
+                if (s < p.ksplit) {
+                  g = __fadd_rn(g, ga[s]);
+                  u = __fadd_rn(u, ua[s]);
+                }
               }
+              acc0[0] = g;
+              acc1[0] = u;
             }
-            gv[c] = g;
-            uv[c] = u;
+            rotate_tokens(acc0, trips);
+            rotate_tokens(acc1, trips);
           }
         }
         // SwiGLU per (j, token), then the token's 1x128 amax over the 128 lanes j
         float* r = red + half * (4 * 16);
 #pragma unroll 1
-        for (int c = 0; c < ntok; ++c) {
-          float h = s_swiglu(bf16_round(gv[c]), bf16_round(uv[c]), p.clamp_mode, p.clamp_limit);
-          if (p.numerics == MOE_NUMERICS_RECIPROCAL) h = bf16_round(h);
-          gv[c] = h;
-          float m = fabsf(h);
+        for (int c = 0; c < trips; ++c) {
+          if (c < ntok) {
+            float h = s_swiglu(bf16_round(acc0[0]), bf16_round(acc1[0]), p.clamp_mode,
+                               p.clamp_limit);
+            if (p.numerics == MOE_NUMERICS_RECIPROCAL) h = bf16_round(h);
+            acc0[0] = h;
+            float m = fabsf(h);
 #pragma unroll
-          for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
-          if (lane == 0) r[q * 16 + c] = m;
+            for (int d = 16; d >= 1; d >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, d));
+            if (lane == 0) r[q * 16 + c] = m;
+          }
+          rotate_tokens(acc0, trips);
+          rotate_tokens(acc1, trips);
         }
         named_barrier_sync(2 + half, 128);
 #pragma unroll 1
-        for (int c = 0; c < ntok; ++c) {
-          const float amax = fmaxf(fmaxf(r[c], r[16 + c]), fmaxf(r[32 + c], r[48 + c]));
-          float inv;
-          const float s = group_scale_numerics(amax, p.act_fmt, p.numerics, &inv);
-          const int row = w.row0 + half * 16 + c;
-          p.a2_q[(size_t)row * I + w.nb * kGroup + j] =
-              (uint8_t)(cvt_e4m3x2(quant_div(gv[c], s, inv), 0.0f) & 0xFF);
-          if (j == 0)
-            store_scale(p.a2_s, (size_t)w.nb * p.R_cap + row, s, p.act_fmt == MOE_SCALE_UE8M0);
+        for (int c = 0; c < trips; ++c) {
+          if (c < ntok) {
+            const float amax = fmaxf(fmaxf(r[c], r[16 + c]), fmaxf(r[32 + c], r[48 + c]));
+            float inv;
+            const float s = group_scale_numerics(amax, p.act_fmt, p.numerics, &inv);
+            const int row = w.row0 + half * 16 + c;
+            p.a2_q[(size_t)row * I + w.nb * kGroup + j] =
+                (uint8_t)(cvt_e4m3x2(quant_div(acc0[0], s, inv), 0.0f) & 0xFF);
+            if (j == 0)
+              store_scale(p.a2_s, (size_t)w.nb * p.R_cap + row, s, p.act_fmt == MOE_SCALE_UE8M0);
+          }
+          rotate_tokens(acc0, trips);
         }
         named_barrier_sync(2 + half, 128);
       } else {

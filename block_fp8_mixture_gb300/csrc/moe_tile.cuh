@@ -29,6 +29,19 @@ __device__ __forceinline__ Item decode_item(const GemmParams& p, int item) {
   return it;
 }
 
+// Whether another row tile of the item's expert reads the same weight blocks.  Its weight copies
+// then keep normal L2 priority, so the other tiles find them there; a lone tile streams them
+// once, with evict-first, so that they do not push its activation rows out of L2.
+__device__ __forceinline__ bool expert_weights_shared(const GemmParams& p, const Item& w,
+                                                      int num_tiles) {
+  auto expert_of = [&](int t) {
+    const int m0 = p.tile_row0 != nullptr ? p.tile_row0[t] : t * kBM;
+    return p.tile_expert[m0 / kBM];
+  };
+  return (w.tile > 0 && expert_of(w.tile - 1) == w.e) ||
+         (w.tile + 1 < num_tiles && expert_of(w.tile + 1) == w.e);
+}
+
 // Weight block-scale rows of an item (indices into the [E][row blocks][K/128] scale array).
 // FC1: the gate block nb and the up block I/128 + nb.  FC2: hidden blocks 2nb and 2nb + 1.
 template <bool kFC1>
