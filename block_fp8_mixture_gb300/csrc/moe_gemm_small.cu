@@ -181,10 +181,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
+  // The routing metadata (chunk list, tile experts, live ends) is written by the alignment, which
+  // completed before the kernel launched ahead of this one finished its own dependency wait (the
+  // activation quantization before FC1, FC1 before FC2).  So the first work item is decoded while
+  // that kernel still runs; only the activation codes and scales the copies read need the wait.
+  const int total = *p.num_chunks * p.n_blocks * p.ksplit;
+  Chunk first = {};
+  if ((int)blockIdx.x < total) first = decode_chunk(p, blockIdx.x);
   grid_dep_wait();                 // the previous kernel's outputs are complete from here on
   grid_dep_launch_dependents();
 
-  const int total = *p.num_chunks * p.n_blocks * p.ksplit;
   const int KB = p.K / kBK;
   const int kb_per_split = KB / p.ksplit;
   const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
@@ -200,7 +206,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     bool ok = true;
     const uint64_t pol_w = policy_evict_first();
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-      const Chunk w = decode_chunk(p, item);
+      const Chunk w = item == (int)blockIdx.x ? first : decode_chunk(p, item);
       int brow0, sr0, sr1;
       bool second;
       if (kFC1) {
@@ -259,7 +265,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     int sc = 0, it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-      const int kb0 = decode_chunk(p, item).ks * kb_per_split;
+      const int kb0 = (item == (int)blockIdx.x ? first : decode_chunk(p, item)).ks * kb_per_split;
       for (int kbs = kb0; ok && kbs < kb0 + kb_per_split; kbs += kSPK) {
         const int nv = min(kSPK, kb0 + kb_per_split - kbs);
         const int s = sc % kSStages;
@@ -305,7 +311,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     int it = 0;
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
-      const Chunk w = decode_chunk(p, item);
+      const Chunk w = item == (int)blockIdx.x ? first : decode_chunk(p, item);
       const int ntok = max(0, min(16, w.live - half * 16));   // live tokens of this half
       int sr0, sr1;
       bool has1;
