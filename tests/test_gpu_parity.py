@@ -201,14 +201,17 @@ def test_layer_empty_and_dropped():
     assert bool((out.view(torch.int16) == -1).all())
 
 
-@pytest.mark.parametrize("name,M", [("glm_slice", 64), ("mid", 128)])
+@pytest.mark.parametrize("name,M", [("glm_slice", 1), ("glm_slice", 8), ("glm_slice", 64),
+                                    ("mid", 1), ("mid", 8), ("mid", 32), ("mid", 128)])
 def test_layer_mid_sizes_full(name, M):
+    """Every sweep point of the two swept workloads up to M=128, all tokens checked."""
     _layer_check(synth.make_case(name, M))
 
 
 @pytest.mark.parametrize("name,M_cap,n", [("padded", 4096, 4096), ("glm_slice", 4096, 4096),
                                           ("mid", 8192, 8192), ("glm_slice", 1024, 1024),
-                                          ("mid", 2048, 2048)])
+                                          ("mid", 2048, 2048), ("glm_slice", 256, 256),
+                                          ("mid", 512, 512)])
 def test_layer_large_sampled(name, M_cap, n):
     case = synth.make_case(name, M_cap, n)
     tokens = np.random.default_rng(M_cap).choice(n, 6, replace=False)
