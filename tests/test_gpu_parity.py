@@ -241,6 +241,34 @@ def test_deterministic():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
+@pytest.mark.parametrize("name,M,n", [("decode", 1, 1), ("decode", 4, 4), ("decode", 32, 29),
+                                      ("mid", 128, 128), ("glm_slice", 1024, 1000)])
+def test_step_entry_points_match_forward(name, M, n):
+    """The five per-step entry points run back to back give the whole-layer forward's output bit for
+    bit (small-batch schedule for the decode and mid cases, 128-row tiles for glm_slice)."""
+    case = synth.make_case(name, M, n)
+    sh = case.shape
+    dev = device_case(case)
+    o_fwd, ws_fwd, _ = run_forward(case, dev)
+    ws = moe.alloc_workspace(M, sh.E, sh.H, sh.I, sh.topk, sh.act_fmt)
+    ws.fill_(0xFF)
+    out = torch.empty((M, sh.H), dtype=torch.bfloat16, device="cuda")
+    out.view(torch.int16).fill_(-1)
+    args = moe.make_args(dev["x"], dev["ids"], dev["w"], dev["w13"], dev["s13"], dev["w2"], dev["s2"],
+                         out, E=sh.E, H=sh.H, I=sh.I, topk=sh.topk, M_cap=M, d_num_tokens=dev["n"],
+                         weight_fmt=sh.weight_fmt, act_fmt=sh.act_fmt, clamp_mode=sh.clamp_mode,
+                         clamp_limit=sh.limit, numerics=sh.numerics)
+    moe.align(dev["ids"], sh.E, sh.H, sh.I, ws, d_num_tokens=dev["n"], act_fmt=sh.act_fmt)
+    moe.quant_act(dev["x"], sh.topk, sh.E, sh.I, ws, d_num_tokens=dev["n"], act_fmt=sh.act_fmt,
+                  numerics=sh.numerics)
+    moe.fc1_swiglu_quant(args, ws)
+    moe.fc2(args, ws)
+    moe.topk_reduce(args, ws)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws_fwd) == 0 and moe.last_device_status(ws) == 0
+    assert torch.equal(o_fwd[:n].view(torch.int16), out[:n].view(torch.int16))
+
+
 def test_graph_replay_changing_routing():
     """Capture once, then change routing and the live-token count in place between replays."""
     shape = synth.small_shape("graph", E=16, H=512, I=256, topk=4)
