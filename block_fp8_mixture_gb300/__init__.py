@@ -91,6 +91,7 @@ SIGNATURES = {
     "moe_batched_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "moe_fp8_batched_forward": (_I, [_P(BatchedArgs), _VP, _SZ, _VP]),
     "moe_last_device_status": (_I, [_VP, _VP]),
+    "moe_selftest_wait_timeout": (_I, [_VP, _I, _VP]),
     "moe_status_str": (ctypes.c_char_p, [_I]),
     "moe_version": (ctypes.c_char_p, []),
 }
@@ -285,6 +286,13 @@ def batched_forward(x, d_counts, w13, s13, w2, s2, out, workspace, *, weight_fmt
 
 def last_device_status(workspace, stream=None) -> int:
     return load_library().moe_last_device_status(_ptr(workspace), _stream(stream))
+
+
+def selftest_wait_timeout(workspace, limit_us: int, stream=None):
+    """Run the bounded-wait diagnostic: a device wait that nothing completes runs out after
+    `limit_us` and records MOE_ERR_DEVICE_TIMEOUT in the workspace status word."""
+    _check(load_library().moe_selftest_wait_timeout(_ptr(workspace), int(limit_us), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 class MoELayer:

@@ -20,7 +20,7 @@ LIBPATH = os.path.join(LIBDIR, LIBNAME)
 BUILD_DIR = os.path.join(os.path.dirname(PKG), "_build")
 
 SOURCES = ["moe_api.cu", "moe_align.cu", "moe_quant.cu", "moe_gemm.cu", "moe_gemm_bs.cu",
-           "moe_gemm_small.cu", "moe_static.cu"]
+           "moe_gemm_small.cu", "moe_static.cu", "moe_diag.cu"]
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-O3", "-lineinfo", "-std=c++17",

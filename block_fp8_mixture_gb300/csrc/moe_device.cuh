@@ -76,11 +76,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 }
 
 // Bounded wait for the phase of `bar` with the given parity to complete.  Gives up when the CTA's
-// abort flag is raised by another role or after kWaitLimitNs; on expiry it raises the abort flag
-// and records MOE_ERR_DEVICE_TIMEOUT in the global status word.  Returns true when the phase
-// completed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                          int* status) {
+// abort flag is raised by another role or after limit_ns (kWaitLimitNs in the layer kernels); on
+// expiry it raises the abort flag and records MOE_ERR_DEVICE_TIMEOUT in the global status word.
+// Returns true when the phase completed.
+__device__ __forceinline__ bool mbar_wait_limit(uint32_t bar, uint32_t parity,
+                                                volatile int* abort_flag, int* status,
+                                                uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   while (true) {
@@ -88,12 +89,17 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
     for (int i = 0; i < 32; ++i)
       if (mbar_try_wait(bar, parity)) return true;
     if (*abort_flag) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) {
+    if (global_timer_ns() - t0 > limit_ns) {
       *abort_flag = 1;
       atomicCAS(status, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
       return false;
     }
   }
+}
+
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                          int* status) {
+  return mbar_wait_limit(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
 // ---------------------------------------------------------------------- TMA

@@ -249,6 +249,16 @@ moe_status moe_fp8_batched_forward(const moe_batched_args* args, void* workspace
 /* Reads the workspace status word (synchronizes `stream` first).  MOE_OK or MOE_ERR_DEVICE_TIMEOUT. */
 moe_status moe_last_device_status(const void* workspace, moe_stream_t stream);
 
+/* Diagnostic of the bounded device-side waits.  Launches one CTA on `stream` that waits, with the
+ * helper every TMA/MMA pipeline of the library uses, for an mbarrier phase that nothing completes,
+ * and gives up after `limit_us` microseconds (1 to 1000000).  The expiry is recorded as in the layer
+ * kernels: the workspace status word (its first int32) becomes MOE_ERR_DEVICE_TIMEOUT unless it
+ * already holds an error, and moe_last_device_status returns it.  The kernel then returns normally
+ * and the context stays usable; the next layer call's alignment resets the word.  Nothing else in
+ * the workspace is touched.  MOE_ERR_INVALID_ARG for a null or not 256-byte-aligned workspace or a
+ * limit out of range; MOE_ERR_CUDA if the launch fails. */
+moe_status moe_selftest_wait_timeout(void* workspace, int limit_us, moe_stream_t stream);
+
 /* Human-readable name of a status. */
 const char* moe_status_str(moe_status status);
 

@@ -107,6 +107,11 @@ def test_forward_validates_before_launch(lib):
     assert lib.moe_align(None, None, 16, 2, 8, 0, 512, 256, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
     assert lib.moe_quant_act(None, None, 16, 8, 512, 256, 2, 0, 0, ws, need, None) == moe.MOE_ERR_INVALID_ARG
     assert fwd(ctypes.byref(_args(numerics=2)), ws, need, None) == moe.MOE_ERR_INVALID_ARG
+    wt = lib.moe_selftest_wait_timeout
+    assert wt(None, 100, None) == moe.MOE_ERR_INVALID_ARG
+    assert wt(ws + 16, 100, None) == moe.MOE_ERR_INVALID_ARG
+    assert wt(ws, 0, None) == moe.MOE_ERR_INVALID_ARG
+    assert wt(ws, 1000001, None) == moe.MOE_ERR_INVALID_ARG
 
 
 def test_missing_library_fails_loudly(monkeypatch, tmp_path):

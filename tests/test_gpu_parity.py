@@ -269,6 +269,23 @@ def test_step_entry_points_match_forward(name, M, n):
     assert torch.equal(o_fwd[:n].view(torch.int16), out[:n].view(torch.int16))
 
 
+def test_bounded_wait_expiry_reported_and_context_usable():
+    """A device wait that nothing completes runs out (the pipelines' bounded-wait helper with a 2 ms
+    limit), the status word reads MOE_ERR_DEVICE_TIMEOUT, and the next forward on the same
+    workspace runs, resets the word and reproduces the earlier output."""
+    case = synth.make_case("decode", 4)
+    dev = device_case(case)
+    o1, ws, _ = run_forward(case, dev)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    moe.selftest_wait_timeout(ws, 2000)
+    assert moe.last_device_status(ws) == moe.MOE_ERR_DEVICE_TIMEOUT
+    o2, _, _ = run_forward(case, dev, ws=ws, poison=False)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+
+
 def test_graph_replay_changing_routing():
     """Capture once, then change routing and the live-token count in place between replays."""
     shape = synth.small_shape("graph", E=16, H=512, I=256, topk=4)
