@@ -58,6 +58,9 @@ SHAPES = {
                          limit=7.0, cfg_id=2),
     "padded": LayerShape("padded", 32, 7168, 2048, 8, act_fmt=SCALE_UE8M0,
                          weight_fmt=SCALE_UE8M0, cfg_id=3),
+    # the same layer with FP32 128x128 weight scales and FP32 1x128 activation scales (the pages
+    # also time this shape with plain FP32 scales)
+    "padded_fp32": LayerShape("padded_fp32", 32, 7168, 2048, 8, cfg_id=3),
     "glm_slice": LayerShape("glm_slice", 256, 6144, 256, 8, routing="zipf", cfg_id=4),
     "mid": LayerShape("mid", 128, 2048, 768, 8, routing="softmax", outliers=0.01, cfg_id=5),
 }
@@ -67,6 +70,7 @@ SWEEPS = {
     "tiny": [(16, 16)],
     "decode": [(1, 1), (4, 4), (32, 32)],
     "padded": [(512, 16), (4096, 4096)],
+    "padded_fp32": [(512, 16), (4096, 4096)],
     "glm_slice": [(m, m) for m in (1, 8, 64, 256, 1024, 4096)],
     "mid": [(m, m) for m in (1, 8, 32, 128, 512, 2048, 8192)],
 }

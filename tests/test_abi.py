@@ -128,3 +128,26 @@ def test_expert_slices_partition_the_experts():
             covered = [e for first, count in spans for e in range(first, first + count)]
             assert covered == list(range(E))
             assert max(c for _, c in spans) - min(c for _, c in spans) <= 1
+
+
+def test_weight_bytes_per_expert_match_printed_figure():
+    """The byte count of the roofline (bench.layer_work) charges each occupied expert its W13 and W2
+    codes plus block scales; for two experts of H=7168, I=2048 the pages print about 88 MB of
+    weights (tests/golden/expert_weight_bytes.json)."""
+    import json
+    import types
+
+    import numpy as np
+
+    import bench
+    import synth
+    g = json.load(open(os.path.join(ROOT, "tests", "golden", "expert_weight_bytes.json")))
+    shape = synth.LayerShape("g", 32, g["H"], g["I"], 8)
+    case = types.SimpleNamespace(shape=shape, n=1,
+                                 topk_ids=np.arange(g["experts"], dtype=np.int32)[None, :])
+    work = bench.layer_work(case)
+    assert work["occupied_experts"] == g["experts"]
+    weights = work["layer_bytes"] - 4 * g["H"] - 8 * shape.topk
+    codes = g["experts"] * 3 * g["H"] * g["I"]
+    assert round(codes / 1e6) == g["printed_mb"]
+    assert codes <= weights <= codes * 1.001       # the block scales add under 0.1%

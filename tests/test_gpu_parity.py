@@ -185,8 +185,9 @@ def test_layer_decode(M):
     _layer_check(synth.make_case("decode", M))
 
 
-def test_layer_padded_16_live():
-    _layer_check(synth.make_case("padded", 512, 16))
+@pytest.mark.parametrize("name", ["padded", "padded_fp32"])
+def test_layer_padded_16_live(name):
+    _layer_check(synth.make_case(name, 512, 16))
 
 
 def test_layer_empty_and_dropped():
@@ -208,7 +209,8 @@ def test_layer_mid_sizes_full(name, M):
     _layer_check(synth.make_case(name, M))
 
 
-@pytest.mark.parametrize("name,M_cap,n", [("padded", 4096, 4096), ("glm_slice", 4096, 4096),
+@pytest.mark.parametrize("name,M_cap,n", [("padded", 4096, 4096), ("padded_fp32", 4096, 4096),
+                                          ("glm_slice", 4096, 4096),
                                           ("mid", 8192, 8192), ("glm_slice", 1024, 1024),
                                           ("mid", 2048, 2048), ("glm_slice", 256, 256),
                                           ("mid", 512, 512)])
