@@ -472,7 +472,8 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.SHAPES),
                     help="layer shape (default: the decode layer the metric is quoted on)")
     ap.add_argument("--M", type=int, default=None, help="token capacity of the headline point")
-    ap.add_argument("--n", type=int, default=None, help="live tokens (default: M)")
+    ap.add_argument("--n", type=int, default=None,
+                    help="live tokens at --M (default: the workload's live count for M, else M)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep", action="store_true",
                     help="also measure every M of the workload's sweep (the decode workload always does)")
@@ -483,8 +484,8 @@ def main():
     args.warmup = max(3, args.warmup)
     if args.M is None:
         args.M = {"decode": 32, "tiny": 16}.get(args.workload, 4096)
-    if args.n is None:
-        args.n = args.M
+    if args.n is None:   # the workload's live count at this capacity (16 of 512 for padded)
+        args.n = dict(synth.SWEEPS.get(args.workload, [])).get(args.M, args.M)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     if args.impl == "reference":
