@@ -168,6 +168,18 @@ def ncu_traffic(key: str):
 FMT_NAMES = {0: "fp32", 1: "fp32-pow2", 2: "ue8m0"}
 
 
+def launches_per_forward(case: synth.LayerCase) -> int:
+    """Kernels one layer forward launches: alignment (plus its per-CTA counting kernel when the
+    plan aligns with several CTAs), quantization, FC1, the SwiGLU + requantization kernel of the
+    FP32-scale tile schedule, FC2 and the top-k reduction."""
+    import block_fp8_mixture_gb300 as moe
+    sh = case.shape
+    plan = moe.workspace_plan(case.M_cap, sh.E, sh.H, sh.I, sh.topk, sh.act_fmt)
+    block_scaled = sh.weight_fmt == synth.SCALE_UE8M0 and sh.act_fmt == synth.SCALE_UE8M0
+    split_swiglu = plan["small_batch"] == 0 and plan["g1"] != 0 and not block_scaled
+    return 5 + (plan["align_ctas"] > 1) + split_swiglu
+
+
 def workload_name(shape, M, n):
     live = f"M={M}" if n == M else f"capacity {M}, {n} live"
     return f"{shape.name} MoE layer E={shape.E} H={shape.H} I={shape.I} top-{shape.topk} {live}"
@@ -411,7 +423,7 @@ def run_ours(args, rank, world):
                 "api": "MoELayer.__call__ (C ABI moe_fp8_block_forward); x, ids and routing "
                        "weights copied in from one pinned staging buffer, the output copied back "
                        "to pinned memory"},
-        "gpu_launches": len(KERNELS) * args.steps,
+        "gpu_launches": launches_per_forward(benches[args.M].case) * args.steps,
         "clocks": clocks,
         "timed_wall_s": wall,
     }
