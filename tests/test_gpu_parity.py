@@ -145,6 +145,21 @@ def test_layer_small_variants(clamp_mode, limit, act_fmt):
     _layer_check(synth.make_case("small_v", 40, 33, shape=shape))
 
 
+@pytest.mark.parametrize("E,H,I,topk,M,n", [
+    (12, 384, 384, 3, 40, 37),    # small-batch: odd 128-column block counts in H (FC2's last item
+                                  # has one weight half) and in I (FC1 column blocks)
+    (24, 640, 128, 1, 96, 90),    # top-1 routing, one FC1 column block, five FC2 blocks
+    (64, 256, 256, 16, 48, 45),   # the largest supported top-k (16 pairs a token)
+    (20, 384, 640, 16, 96, 96),   # top-16 on the 128-row tiles (1536 pairs > 16 E)
+])
+def test_layer_odd_blocks_and_topk_extremes(E, H, I, topk, M, n):
+    shape = synth.small_shape("edge", E=E, H=H, I=I, topk=topk)
+    case = synth.make_case("edge", M, n, shape=shape)
+    small = moe.workspace_plan(M, E, H, I, topk)["small_batch"]
+    assert small == (1 if M * topk <= 16 * E else 0)
+    _layer_check(case)
+
+
 @pytest.mark.parametrize("clamp_mode,limit", [(0, 0.0), (1, 0.02), (2, 0.01)])
 @pytest.mark.parametrize("act_fmt,weight_fmt", [(0, 0), (1, 0), (2, 2)])
 def test_layer_tile_kernel_variants(clamp_mode, limit, act_fmt, weight_fmt):
