@@ -160,6 +160,20 @@ def test_layer_odd_blocks_and_topk_extremes(E, H, I, topk, M, n):
     _layer_check(case)
 
 
+@pytest.mark.parametrize("E,H,I,topk,M,n,small,ksplit", [
+    (2, 32768, 128, 1, 8, 8, 1, 8),       # largest H: 256 K blocks, FC1 split 8 ways (the most)
+    (2, 32768, 128, 1, 64, 60, 0, 1),     # largest H on the 128-row tiles
+    (2, 128, 16384, 1, 8, 7, 1, 1),       # largest I: 128 FC1 column blocks, FC2 K = 16384
+    (2, 128, 16384, 1, 64, 64, 0, 1),     # largest I on the 128-row tiles
+    (1024, 256, 128, 8, 16, 16, 1, 1),    # largest expert count
+])
+def test_layer_maximum_dimensions(E, H, I, topk, M, n, small, ksplit):
+    plan = moe.workspace_plan(M, E, H, I, topk)
+    assert (plan["small_batch"], plan["fc1_ksplit"]) == (small, ksplit)
+    shape = synth.small_shape("maxd", E=E, H=H, I=I, topk=topk)
+    _layer_check(synth.make_case("maxd", M, n, shape=shape))
+
+
 @pytest.mark.parametrize("clamp_mode,limit", [(0, 0.0), (1, 0.02), (2, 0.01)])
 @pytest.mark.parametrize("act_fmt,weight_fmt", [(0, 0), (1, 0), (2, 2)])
 def test_layer_tile_kernel_variants(clamp_mode, limit, act_fmt, weight_fmt):
