@@ -160,6 +160,24 @@ def test_layer_odd_blocks_and_topk_extremes(E, H, I, topk, M, n):
     _layer_check(case)
 
 
+@pytest.mark.parametrize("name,M", [("decode", 32), ("mid", 512)])
+def test_layer_zero_and_duplicate_tokens(name, M):
+    """Degenerate tokens, exactly: an all-zero x row quantizes to the floor scale and zero codes and
+    gives an all-zero output row; two tokens with the same x and the same routing give identical
+    output rows although their pairs sit in different rows of the expert segments."""
+    case = synth.make_case(name, M)
+    case.x_bits[3] = 0
+    case.x[3] = 0.0
+    case.x_bits[7] = case.x_bits[11]
+    case.x[7] = case.x[11]
+    case.topk_ids[7] = case.topk_ids[11]
+    case.topk_weights[7] = case.topk_weights[11]
+    _, out = _layer_check(case, tokens=[0, 3, 7, 11, M - 1])
+    rows = out.view(torch.int16).cpu().numpy()
+    assert not rows[3].any()
+    assert np.array_equal(rows[7], rows[11])
+
+
 @pytest.mark.parametrize("E,H,I,topk,M,n,small,ksplit", [
     (2, 32768, 128, 1, 8, 8, 1, 8),       # largest H: 256 K blocks, FC1 split 8 ways (the most)
     (2, 32768, 128, 1, 64, 60, 0, 1),     # largest H on the 128-row tiles
