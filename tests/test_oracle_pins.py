@@ -222,6 +222,116 @@ def test_quant_1x128_properties():
             assert np.all(top[s > oracle.SCALE_FLOOR] == 448.0)
 
 
+# ---------------------------------------------- quantizer, element by element
+def _expected_scale(amax: float, fmt) -> float:
+    """The group scale from its definition, in exact rationals: max(RN32(amax/448), RN32(1/229376)),
+    then, for the power-of-two formats, the smallest power of two that is >= it."""
+    s = max(exact_round_f32(Fraction(amax) / 448), exact_round_f32(Fraction(1, 229376)))
+    if fmt in (oracle.SCALE_FP32_POW2, oracle.SCALE_UE8M0):
+        e = 0
+        while Fraction(2) ** e < Fraction(s):
+            e += 1
+        while Fraction(2) ** (e - 1) >= Fraction(s):
+            e -= 1
+        s = 2.0 ** e
+    return s
+
+
+def _nearest_code(q: Fraction, sign_of: float) -> int:
+    """E4M3 code of RN32(q): the quotient or product rounded once to fp32, then to the nearest code."""
+    r = exact_round_f32(q)
+    if r == 0.0:
+        r = math.copysign(0.0, sign_of)
+    return brute_nearest_e4m3(r)
+
+
+def _quant_pin_inputs():
+    """BF16 groups of 128 chosen to expose the quantizer's arithmetic.
+
+    Midpoint groups: amax = 448 * c * 2^j makes the scale exactly c * 2^j, and every other element
+    is c * 2^j times an E4M3 midpoint (all BF16 values), so x / scale lands exactly on a tie, which
+    goes to the even code; with c = 7 the product x * RN32(1/scale) is one fp32 ulp off the tie for
+    about a quarter of them and picks the other code (the TensorRT-LLM page's reason for correctly
+    rounded division: BF16 inputs that sit on E4M3 midpoints).  Then random BF16 groups, a group
+    with 1% outliers x10, an all-zero group and a tiny group (both at the scale floor)."""
+    pos = fm.E4M3_VALUES[:0x7F]
+    mids = (pos[:-1] + pos[1:]) / 2.0                    # 126 positive midpoints
+    groups = []
+    for c, j in ((7, -8), (7, 3), (3, -5), (5, 0)):
+        unit = c * 2.0 ** j
+        for sign in (1.0, -1.0):
+            g = np.zeros(128, np.float64)
+            g[0] = 448.0 * unit
+            g[1:127] = sign * mids * unit
+            g[127] = -sign * mids[60] * unit
+            groups.append(g)
+    rng = np.random.default_rng(31)
+    for _ in range(8):
+        groups.append(rng.standard_normal(128) * 3.0)
+    out = rng.standard_normal(128)
+    out[rng.uniform(size=128) < 0.05] *= 10.0
+    groups.append(out)
+    groups.append(np.zeros(128))
+    groups.append(rng.standard_normal(128) * 1e-6)
+    v = np.stack(groups).astype(F32)
+    bv = fm.bf16_round(v)
+    assert np.array_equal(bv[:8], v[:8])                # the designed groups are BF16 exactly
+    return bv
+
+
+def _quant_mismatches(quant, v, fmt, numerics=oracle.NUMERICS_DIVIDE):
+    """Elements whose code or group scale differs from the definition evaluated in exact rationals."""
+    q, s = quant(v, fmt, numerics)
+    bad = 0
+    for gi in range(v.shape[0]):
+        row = v[gi].tolist()
+        amax = max(abs(x) for x in row)
+        if numerics == oracle.NUMERICS_RECIPROCAL and fmt == oracle.SCALE_FP32:
+            inv = 448.0 * 512.0 if amax == 0 else min(exact_round_f32(Fraction(448) / Fraction(amax)),
+                                                      448.0 * 512.0)
+            want_s = exact_round_f32(1 / Fraction(inv))
+            codes = [_nearest_code(Fraction(x) * Fraction(inv), x) for x in row]
+        else:
+            want_s = _expected_scale(amax, fmt)
+            codes = [_nearest_code(Fraction(x) / Fraction(want_s), x) for x in row]
+        bad += int(float(s[gi, 0]) != want_s) * 128
+        bad += sum(int(a != b) for a, b in zip(q[gi].tolist(), codes))
+    return bad
+
+
+@pytest.mark.parametrize("fmt", [oracle.SCALE_FP32, oracle.SCALE_FP32_POW2, oracle.SCALE_UE8M0])
+def test_quant_1x128_element_by_element(fmt):
+    """Every code is the nearest E4M3 (ties to even) of x / scale correctly rounded to fp32, and
+    every scale is max(RN32(amax/448), RN32(1/229376)) (power of two rounded up for POW2/UE8M0),
+    both evaluated in exact rationals (vLLM per-layer scale page, Details: x/scale; TensorRT-LLM
+    page, rounding-fix commit: correctly rounded division)."""
+    v = _quant_pin_inputs()
+    assert _quant_mismatches(oracle.quant_1x128, v, fmt) == 0
+    if fmt == oracle.SCALE_UE8M0:
+        _, s = oracle.quant_1x128(v, fmt)
+        assert np.array_equal(oracle.scale_bytes(s),
+                              np.array([[127 + int(math.log2(float(x)))] for x in s[:, 0]], np.uint8))
+
+
+def test_quant_1x128_reciprocal_element_by_element():
+    """The TensorRT-LLM numerics: codes are the nearest E4M3 of x * RN32(448/amax) rounded once to
+    fp32, the stored scale is RN32(1/inv), with inv capped at 448*512 (the scale floor)."""
+    v = _quant_pin_inputs()
+    assert _quant_mismatches(oracle.quant_1x128, v, oracle.SCALE_FP32, oracle.NUMERICS_RECIPROCAL) == 0
+
+
+def test_quant_pin_catches_reciprocal_multiply():
+    """A quantizer that multiplies by RN32(1/scale) instead of dividing by the scale (the mistake the
+    TensorRT-LLM page's rounding fix removes) fails the element-by-element pin."""
+    def planted(v, fmt, numerics=0):
+        g = np.asarray(v, F32).reshape(v.shape[0], -1, 128)
+        s = oracle.group_scale(np.abs(g).max(-1), fmt)
+        inv = (F32(1.0) / s).astype(F32)
+        return fm.e4m3_encode((g * inv[..., None]).astype(F32)).reshape(v.shape), s
+    v = _quant_pin_inputs()
+    assert _quant_mismatches(planted, v, oracle.SCALE_FP32) > 0
+
+
 def test_quant_scaling_by_power_of_two():
     rng = np.random.default_rng(7)
     v = rng.standard_normal((3, 256)).astype(F32)
@@ -342,6 +452,64 @@ def test_swiglu_against_high_precision():
         assert abs(hi - float(exact)) <= 4 * 2.0 ** -24 * abs(float(exact)) + 1e-45
 
 
+def _mp_fraction(x) -> Fraction:
+    """An mpmath number as an exact rational (mantissa * 2^exponent)."""
+    import mpmath
+    man, exp = mpmath.mpf(x).man_exp
+    return Fraction(int(man)) * Fraction(2) ** int(exp)
+
+
+def _swiglu_steps(g: float, u: float, clamp_mode=0, limit=0.0) -> float:
+    """SiLU(g)*up, each stated step rounded once to fp32, in exact rationals: e = RN32(exp(-g)) (exp
+    to 120 bits, then rounded), d = RN32(1 + e), sig = RN32(1/d) (IEEE division), silu = RN32(g*sig),
+    h = RN32(silu*u); the clamps are exact (TensorRT-LLM page, human review: 1/(1+expf(-x)) with
+    IEEE division)."""
+    import mpmath
+    mpmath.mp.prec = 120
+    if clamp_mode == oracle.CLAMP_BEFORE_SILU:
+        g = min(g, limit)
+        u = min(max(u, -limit), limit)
+    e = exact_round_f32(_mp_fraction(mpmath.exp(-mpmath.mpf(g))))
+    d = exact_round_f32(1 + Fraction(e))
+    sig = exact_round_f32(1 / Fraction(d))
+    silu = exact_round_f32(Fraction(g) * Fraction(sig))
+    if clamp_mode == oracle.CLAMP_AFTER_SILU:
+        silu = min(silu, limit)
+        u = min(max(u, -limit), limit)
+    return exact_round_f32(Fraction(silu) * Fraction(u))
+
+
+def _swiglu_pin_inputs():
+    rng = np.random.default_rng(41)
+    g = fm.bf16_round((rng.standard_normal(1500) * 4).astype(F32))
+    u = fm.bf16_round((rng.standard_normal(1500) * 4).astype(F32))
+    return g, u
+
+
+def _swiglu_mismatches(fn, g, u, clamp_mode=0, limit=0.0):
+    h = fn(g, u, clamp_mode, limit)
+    return sum(int(float(hi) != _swiglu_steps(gi, ui, clamp_mode, limit))
+               for gi, ui, hi in zip(g.tolist(), u.tolist(), h.tolist()))
+
+
+@pytest.mark.parametrize("clamp_mode,limit", [(0, 0.0), (1, 1.5), (2, 1.5)])
+def test_swiglu_step_by_step(clamp_mode, limit):
+    """Each fp32 step of the SwiGLU equals its exact-rational evaluation, bit for bit."""
+    g, u = _swiglu_pin_inputs()
+    assert _swiglu_mismatches(oracle.swiglu, g, u, clamp_mode, limit) == 0
+
+
+def test_swiglu_pin_catches_a_once_rounded_sigmoid():
+    """A sigmoid formed in float64 and rounded once (instead of the stated fp32 steps) fails the
+    step-by-step pin."""
+    def planted(gate, up, clamp_mode=0, limit=0.0):
+        g = np.asarray(gate, F32)
+        sig = (1.0 / (1.0 + np.exp(-g.astype(np.float64)))).astype(F32)
+        return ((g * sig).astype(F32) * np.asarray(up, F32)).astype(F32)
+    g, u = _swiglu_pin_inputs()
+    assert _swiglu_mismatches(planted, g, u) > 0
+
+
 def test_swiglu_clamp_semantics():
     g = np.array([10.0, -10.0, 3.0, 9.0], F32)
     u = np.array([-9.0, 9.0, 2.0, 1.0], F32)
@@ -369,6 +537,78 @@ def test_topk_reduce_hand_example():
     y = np.array([[[1.0], [2.0 ** -9]]], F32)
     out = oracle.topk_reduce(y, np.ones((1, 2), F32), np.ones((1, 2), bool))
     assert out[0, 0] == 1.0
+
+
+def _reduce_steps(y, w, present, out_fp32=False):
+    """out = RNbf16(acc), acc = 0; for j ascending over present pairs acc = RN32(acc + RN32(w*y)),
+    evaluated with exact rationals (TensorRT-LLM page, rounding-fix commit: the finalize step scales
+    the BF16 expert outputs in fp32)."""
+    T, K, H = y.shape
+    out = np.zeros((T, H), F32)
+    for t in range(T):
+        for h in range(H):
+            acc = 0.0
+            for j in range(K):
+                if present[t, j]:
+                    term = exact_round_f32(Fraction(float(w[t, j])) * Fraction(float(y[t, j, h])))
+                    acc = exact_round_f32(Fraction(acc) + Fraction(term))
+            out[t, h] = acc
+    return out if out_fp32 else fm.bf16_round(out)
+
+
+def _reduce_pin_case():
+    """Terms chosen so that the order and the rounding of the fp32 accumulation decide the result.
+
+    Column 0: 1+2^-8 (a BF16 tie), then 2^-24 twice.  In ascending order each 2^-24 is half an fp32
+    ulp of the running sum and ties back to it, so the sum stays on the BF16 tie and rounds to 1.0;
+    summed in reverse, or in float64 and rounded once, the two small terms survive as 2^-23 and the
+    BF16 result is 1 + 2^-7.  Column 1: a product w*y that is not an fp32 number (its per-term
+    rounding matters), on token 1.  A dropped pair between live ones carries a large value that must not count.
+    Further columns: random BF16 outputs and fp32 weights."""
+    T, K, H = 3, 4, 6
+    rng = np.random.default_rng(43)
+    y = fm.bf16_round(rng.standard_normal((T, K, H)).astype(F32))
+    w = rng.uniform(0.05, 1.0, (T, K)).astype(F32)
+    present = np.ones((T, K), bool)
+    y[0, :, 0] = [1.0, 2.0 ** -24, 1e4, 2.0 ** -24]
+    w[0] = [F32(1 + 2.0 ** -8), 1.0, 1.0, 1.0]
+    present[0, 2] = False
+    y[1, :, 1] = [1.0, fm.bf16_round(np.array([1 + 2.0 ** -7], F32))[0], 3.0, 0.0]
+    w[1, 1] = F32(1 + 2.0 ** -20)
+    present[2, 0] = False
+    return y, w, present
+
+
+def test_topk_reduce_step_by_step():
+    y, w, present = _reduce_pin_case()
+    for out_fp32 in (False, True):
+        got = oracle.topk_reduce(y, w, present, out_fp32)
+        want = _reduce_steps(y, w, present, out_fp32)
+        assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), out_fp32
+    assert oracle.topk_reduce(y, w, present)[0, 0] == 1.0
+
+
+def test_topk_reduce_pin_catches_order_and_fused_accumulation():
+    """Summing j descending, or accumulating in float64 and rounding once, fails the pin."""
+    y, w, present = _reduce_pin_case()
+    want = _reduce_steps(y, w, present)
+
+    def descending(y, w, present):
+        acc = np.zeros((y.shape[0], y.shape[2]), F32)
+        for j in reversed(range(w.shape[1])):
+            term = (w[:, j][:, None] * y[:, j]).astype(F32)
+            acc = np.where(present[:, j][:, None], (acc + term).astype(F32), acc)
+        return fm.bf16_round(acc)
+
+    def fused64(y, w, present):
+        acc = np.zeros((y.shape[0], y.shape[2]), np.float64)
+        for j in range(w.shape[1]):
+            acc += np.where(present[:, j][:, None],
+                            w[:, j][:, None].astype(np.float64) * y[:, j].astype(np.float64), 0.0)
+        return fm.bf16_round(acc.astype(F32))
+
+    for planted in (descending, fused64):
+        assert not np.array_equal(planted(y, w, present), want), planted.__name__
 
 
 # ----------------------------------------------------------- layer pins
