@@ -210,12 +210,16 @@ moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size
  *  - Layers whose moe_workspace_bytes(...) exceeds MOE_STATIC_SCRATCH_BYTES are rejected with
  *    MOE_ERR_WORKSPACE_TOO_SMALL before anything is launched (e.g. single-token decode fits; the
  *    32-token, 288-expert decode layer does not).
- *  - The first call on a device looks up the array's device address (cudaGetSymbolAddress) with
- *    that device current; make that first call before any stream capture.
+ *  - The first call in a context looks up the array's device address (cudaGetSymbolAddress) with
+ *    that device current, and caches it with the context's id; make that first call before any
+ *    stream capture.  After a device reset (a new context) the next call looks the address up again.
  *  - All calls on a device share the array and it keeps the last call's contents; the state that
  *    must start at zero is reset on the GPU by every call.  Calls that overlap on the GPU (other
  *    streams or host threads) race on the array: serialise them.
- *  - The device status word of these calls is not readable through moe_last_device_status. */
+ *  - The device status word of these calls is not readable through moe_last_device_status, so a
+ *    device-side wait that runs out (MOE_ERR_DEVICE_TIMEOUT on the other entry points) is not
+ *    reported by this path: the call has already returned MOE_OK and `out` holds wrong values.
+ *    Callers that need that report use moe_fp8_block_forward with a workspace. */
 moe_status moe_fp8_block_forward_static(const moe_fwd_args* args, moe_stream_t stream);
 
 /* Batched-expert layout (vLLM per-layer scale page, Details, batched experts: per-expert rows with
