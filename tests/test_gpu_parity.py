@@ -256,15 +256,124 @@ def test_layer_mid_sizes_full(name, M):
     _layer_check(synth.make_case(name, M))
 
 
+def covering_tokens(case):
+    """Tokens whose pairs sit on the first and the last live row of every expert segment and of every
+    live 128-row tile (so every tile of every expert, including each expert's partial last tile,
+    and every position of the persistent GEMMs' work lists is checked), found from the oracle's
+    alignment of the same routing."""
+    a = oracle.align(case.topk_ids, case.n, case.shape.E)
+    k = case.shape.topk
+    seg, live, sp = a["seg_start"], a["live_end"], a["sorted_pair"]
+    toks = set()
+    for e in range(case.shape.E):
+        for m0 in range(int(seg[e]), int(live[e]), oracle.ALIGN):
+            last = min(m0 + oracle.ALIGN, int(live[e])) - 1
+            toks.add(int(sp[m0]) // k)
+            toks.add(int(sp[last]) // k)
+    return np.array(sorted(toks), np.int64)
+
+
+def check_a1_bit_exact(case, views, tokens):
+    """FC1-input codes and scales of every pair of the given tokens equal the oracle's, bit for bit."""
+    sh = case.shape
+    k = sh.topk
+    pair_row = views["pair_row"].cpu().numpy()
+    q_ref, s_ref = oracle.quant_1x128(case.x[tokens], sh.act_fmt, sh.numerics)
+    rows, want_q, want_s = [], [], []
+    for i, t in enumerate(tokens):
+        for j in range(k):
+            r = int(pair_row[t * k + j])
+            if 0 <= case.topk_ids[t, j] < sh.E:
+                rows.append(r)
+                want_q.append(q_ref[i])
+                want_s.append(s_ref[i])
+            else:
+                assert r == -1
+    idx = torch.from_numpy(np.array(rows, np.int64)).to(views["a1_q"].device)
+    got_q = views["a1_q"].index_select(0, idx).cpu().numpy()
+    got_s = views["a1_s"].index_select(1, idx).cpu().numpy().T
+    assert np.array_equal(got_q, np.stack(want_q))
+    want_s = np.stack(want_s)
+    if sh.act_fmt == oracle.SCALE_UE8M0:
+        assert np.array_equal(got_s, oracle.scale_bytes(want_s))
+    else:
+        assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32))
+    return len(rows)
+
+
 @pytest.mark.parametrize("name,M_cap,n", [("padded", 4096, 4096), ("padded_fp32", 4096, 4096),
                                           ("glm_slice", 4096, 4096),
                                           ("mid", 8192, 8192), ("glm_slice", 1024, 1024),
                                           ("mid", 2048, 2048), ("glm_slice", 256, 256),
                                           ("mid", 512, 512)])
-def test_layer_large_sampled(name, M_cap, n):
+def test_layer_large_every_tile(name, M_cap, n):
+    """Full-size layers, checked on the tokens that cover the first and last live row of every 128-row
+    tile and every expert segment; their FC1-input codes and scales bit-exact, their FC2-input codes
+    >= 99.9% identical, their outputs within the layer tolerance, and the padding untouched."""
     case = synth.make_case(name, M_cap, n)
-    tokens = np.random.default_rng(M_cap).choice(n, 6, replace=False)
-    _layer_check(case, tokens=tokens)
+    tokens = covering_tokens(case)
+    out, ws, views = run_forward(case)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    assert check_a1_bit_exact(case, views, tokens) > 0
+    gpu = bf16_tensor_to_f32(out)
+    ref, pairs = oracle_forward(case, tokens, return_pairs=True)
+    assert_layer_close(gpu[tokens], ref, f"{name} {M_cap}")
+    assert check_a2_codes(case, views, pairs) >= CODE_MATCH_MIN
+    check_untouched(case, views)
+
+
+def _embed(case, M_big, seed):
+    """The same n live tokens (x rows, ids, routing weights) at a larger token capacity; the rows
+    past n hold other tokens that must never be read."""
+    rng = np.random.default_rng(seed)
+    sh = case.shape
+    big = synth.make_case(sh.name, M_big, case.n, shape=sh, seed=seed, weights=case.weights)
+    big.x_bits[: case.M_cap] = case.x_bits
+    big.x[: case.M_cap] = case.x
+    big.topk_ids[: case.M_cap] = case.topk_ids
+    big.topk_weights[: case.M_cap] = case.topk_weights
+    big.x_bits[case.n:] = rng.integers(0, 2 ** 16, big.x_bits[case.n:].shape).astype(np.uint16)
+    return big
+
+
+@pytest.mark.parametrize("name,M_small,M_big,n", [("padded_fp32", 4096, 8192, 4096),
+                                                  ("padded", 512, 4096, 16),
+                                                  ("decode", 16, 48, 16)])
+def test_capacity_invariance(name, M_small, M_big, n):
+    """The padded capacity never reaches the result (vLLM padded-work page, Validation: outputs
+    identical between schedules, poisoned workspaces): the same live tokens at two capacities that
+    take the same GEMM schedule give byte-identical outputs, and both workspaces keep their
+    poisoned padding."""
+    small = synth.make_case(name, M_small, n)
+    big = _embed(small, M_big, seed=99)
+    sh = small.shape
+    p_s = moe.workspace_plan(M_small, sh.E, sh.H, sh.I, sh.topk, sh.act_fmt)
+    p_b = moe.workspace_plan(M_big, sh.E, sh.H, sh.I, sh.topk, sh.act_fmt)
+    assert (p_s["small_batch"], p_s["fc1_ksplit"]) == (p_b["small_batch"], p_b["fc1_ksplit"])
+    assert p_b["R_cap"] > p_s["R_cap"]
+    out_s, ws_s, v_s = run_forward(small)
+    out_b, ws_b, v_b = run_forward(big)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws_s) == moe.MOE_OK and moe.last_device_status(ws_b) == moe.MOE_OK
+    assert torch.equal(out_s[:n].view(torch.int16), out_b[:n].view(torch.int16))
+    assert bool((out_s[n:].view(torch.int16) == -1).all())
+    assert bool((out_b[n:].view(torch.int16) == -1).all())
+    check_untouched(small, v_s)
+    check_untouched(big, v_b)
+
+
+@pytest.mark.parametrize("name,M", [("decode", 32), ("tiny", 16), ("mid", 512)])
+def test_layer_zero_routing_weights(name, M):
+    """Zero routing weights (TensorRT-LLM page, human review): a zero-weight pair still runs through
+    the experts but contributes exactly nothing; a token whose weights are all zero gets a zero row."""
+    case = synth.make_case(name, M)
+    case.topk_weights[1, :] = 0.0
+    case.topk_weights[2, ::2] = 0.0
+    case.topk_weights[M - 1, -1] = 0.0
+    rel, out = _layer_check(case, tokens=[0, 1, 2, 5, M - 1])
+    rows = out.view(torch.int16).cpu().numpy()
+    assert not rows[1].any()
 
 
 def test_layer_forced_empty_experts():
