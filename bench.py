@@ -1,17 +1,20 @@
 """Benchmark of the block-FP8 MoE layer forward on GB300.
 
-Workload (default): the decode-sized layer -- 288 experts, hidden 4096, intermediate 512, top-8,
-SwiGLU clamped at 7.0, FP8 E4M3 weights with 128x128 fp32 block scales, BF16 activations,
-softmax top-8 routing -- at M = 32 live tokens; the M = 1 and M = 4 points of the same workload
-are measured in the same run ("sweep").  One step = one full layer forward (routing alignment,
-activation quantization, FC1 + SwiGLU + requant, FC2, top-k reduce) replayed from a CUDA graph,
-with L2 flushed (a 512 MB write, larger than the 129 MB L2) before every step; the step time is
-taken with CUDA events around the replay on the launching stream.
+Workload (default): the largest single-GPU layer the metric is quoted on -- 32 experts, hidden
+7168, intermediate 2048, top-8, FP8 E4M3 weights with 128x128 UE8M0 (power-of-two) block scales,
+UE8M0 1x128 activation scales, BF16 activations, softmax top-8 routing -- at a token capacity of
+4096 with all 4096 tokens live.  The same run also measures ("sweep") the decode layer (288 experts,
+hidden 4096, intermediate 512, SwiGLU clamped at 7.0, FP32 scales) at M = 1, 4 and 32, the padded
+layer at capacity 512 with 16 live tokens, and the padded layer with FP32 weight and activation
+scales at 512/16 and 4096/4096.  One step = one full layer forward (routing alignment, activation
+quantization, FC1 + SwiGLU + requant, FC2, top-k reduce) replayed from a CUDA graph, with L2 flushed
+(a 512 MB write, larger than the 129 MB L2) before every step; the step time is taken with CUDA
+events around the replay on the launching stream.
 
 Prints one JSON line.  `--impl reference` times the CPU oracle on the host cores instead (the
-reference arm).  Under torchrun every rank runs its own replica of the layer on its own batch
-(weak scaling: the layer has no exchange step between data-parallel replicas); rank 0 prints the
-max over ranks.
+reference arm).  `--measure-peaks` times the dense FP8 GEMM peak (torch._scaled_mm, e4m3 8192^3).
+Under torchrun every rank runs its own replica of the layer on its own batch (weak scaling: the
+layer has no exchange step between data-parallel replicas); rank 0 prints the max over ranks.
 """
 
 from __future__ import annotations
@@ -34,8 +37,10 @@ sys.path.insert(0, ROOT)
 import synth  # noqa: E402
 
 METRIC = "MoE layer us and % of FP8/HBM roofline vs live tokens M (1 GB300)"
-WORKLOAD = "decode"
-SWEEP_M = (1, 4, 32)
+WORKLOAD = "padded"
+# (workload, token capacity, live tokens) measured beside the headline point
+SWEEP_POINTS = (("decode", 1, 1), ("decode", 4, 4), ("decode", 32, 32), ("padded", 512, 16),
+                ("padded_fp32", 512, 16), ("padded_fp32", 4096, 4096))
 KERNELS = ("align", "quant", "fc1", "fc2", "reduce")
 FLUSH_BYTES = 512 << 20
 
@@ -52,9 +57,16 @@ def load_peaks():
         return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def fp8_peak_tflops(peaks):
-    # dense FP8 = 2x dense BF16 on this part (nominal 4.5 vs 2.25 PFLOP/s)
-    return 2.0 * peaks["bf16_tflops"]
+def fp8_peak(peaks):
+    """Dense FP8 GEMM peak in TFLOP/s and where it comes from: the cuBLASLt e4m3 GEMM measured on this
+    part (profiles/fp8_peak.json, written from `bench.py --measure-peaks`), else twice the measured
+    BF16 peak (nominal 4.5 vs 2.25 PFLOP/s)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "fp8_peak.json")) as f:
+            rec = json.load(f)
+        return float(rec["fp8_tflops"]), "measured: torch._scaled_mm e4m3 8192^3, best of 10 (profiles/fp8_peak.json)"
+    except (OSError, KeyError, ValueError):
+        return 2.0 * peaks["bf16_tflops"], f"{peaks['source']}: 2 x MEASURED_PEAKS bf16_tflops"
 
 
 # ------------------------------------------------------- algorithmic work
@@ -185,6 +197,20 @@ def workload_name(shape, M, n):
     return f"{shape.name} MoE layer E={shape.E} H={shape.H} I={shape.I} top-{shape.topk} {live}"
 
 
+def bench_config(shape, M, n, world):
+    """The `config` object of the JSON line (the same for both arms)."""
+    return {"workload": workload_name(shape, M, n),
+            "clamp": ("none" if shape.clamp_mode == 0 else
+                      f"SwiGLU clamp {shape.limit} {'before' if shape.clamp_mode == 1 else 'after'} SiLU"),
+            "scales": f"weights {FMT_NAMES[shape.weight_fmt]} 128x128, activations {FMT_NAMES[shape.act_fmt]} 1x128",
+            "l2": "flushed before every step (512 MB write)", "timing": "CUDA graph replay, CUDA events",
+            "parallelism": f"replicas x{world}"}
+
+
+def point_key(workload, M, n):
+    return f"{workload} {M}" if n == M else f"{workload} {M}/{n}"
+
+
 # ------------------------------------------------------------ our arm
 class LayerBench:
     def __init__(self, workload, M, n, rank, weights, dev_weights):
@@ -235,34 +261,45 @@ def run_ours(args, rank, world):
         import torch.distributed as dist
         dist.init_process_group("nccl")
     peaks = load_peaks()
-    shape = synth.SHAPES[args.workload]
-    weights = synth.make_weights(shape)
-    dev_w = tuple(torch.from_numpy(a).cuda() for a in (weights.w13, weights.s13, weights.w2, weights.s2))
+    fp8_tflops, fp8_source = fp8_peak(peaks)
+    hbm_peak = peaks["hbm_gbs"]
+    head = (args.workload, args.M, args.n)
+    do_sweep = not (args.no_sweep or args.profile_run)
+    if not do_sweep:
+        points = [head]
+    elif args.sweep:
+        points = [(args.workload, m, n) for m, n in synth.SWEEPS[args.workload]]
+    elif args.workload == WORKLOAD:
+        points = list(SWEEP_POINTS)
+    else:
+        points = []
+    points = [head] + [pt for pt in points if pt != head]
+
+    weights, dev_w = {}, {}
+    for wl, _, _ in points:
+        if wl not in weights:
+            weights[wl] = synth.make_weights(synth.SHAPES[wl])
+            dev_w[wl] = tuple(torch.from_numpy(a).cuda() for a in
+                              (weights[wl].w13, weights[wl].s13, weights[wl].w2, weights[wl].s2))
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device="cuda")
     stream = torch.cuda.Stream()
-    do_sweep = (args.workload == WORKLOAD or args.sweep) and not (args.no_sweep or args.profile_run)
-    sweep_points = SWEEP_M if args.workload == WORKLOAD else [m for m, _ in synth.SWEEPS[args.workload]]
-    sweep = sorted(set(sweep_points) | {args.M}) if do_sweep else [args.M]
-    live = dict(synth.SWEEPS[args.workload])
-    benches = {M: LayerBench(args.workload, M, args.n if M == args.M else live.get(M, M), rank,
-                             weights, dev_w)
-               for M in sweep}
+    benches = {pt: LayerBench(pt[0], pt[1], pt[2], rank, weights[pt[0]], dev_w[pt[0]]) for pt in points}
 
-    # graphs of the whole forward, one per M
+    # graphs of the whole forward, one per point
     graphs = {}
     with torch.cuda.stream(stream):
-        for M, b in benches.items():
+        for pt, b in benches.items():
             b.forward(stream)
             stream.synchronize()
             assert moe.last_device_status(b.ws, stream) == moe.MOE_OK
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
                 b.forward(stream)
-            graphs[M] = g
+            graphs[pt] = g
     torch.cuda.synchronize()
 
-    def timed_graph(M, steps, warmup):
-        g = graphs[M]
+    def timed_graph(pt, steps, warmup):
+        g = graphs[pt]
         times = []
         with torch.cuda.stream(stream):
             for i in range(warmup + steps):
@@ -277,8 +314,8 @@ def run_ours(args, rank, world):
         stream.synchronize()
         return [a.elapsed_time(b) * 1e3 for a, b in times]   # us
 
-    def per_kernel(M, steps):
-        b = benches[M]
+    def per_kernel(pt, steps):
+        b = benches[pt]
         fns = b.steps(stream)
         acc = {k: [] for k in KERNELS}
         with torch.cuda.stream(stream):
@@ -297,11 +334,11 @@ def run_ours(args, rank, world):
                         acc[k].append(a.elapsed_time(c) * 1e3)
         return {k: statistics.mean(v) for k, v in acc.items()}
 
-    def e2e(M, steps, warmup):
+    def e2e(pt, steps, warmup):
         # The step's inputs (x, ids, routing weights) sit in one pinned staging buffer and go to the
         # device in one copy; the layer reads device views of it.  Each part starts on a 256-byte
         # boundary.
-        b = benches[M]
+        b = benches[pt]
         parts = [b.x, b.ids, b.wts]
         offs, size = [], 0
         for t in parts:
@@ -338,19 +375,19 @@ def run_ours(args, rank, world):
         return statistics.mean(times), h2d, d2h
 
     if args.profile_run:
-        us = timed_graph(args.M, args.steps, args.warmup)
-        return {"profile_run": True, "M": args.M, "us_mean": statistics.mean(us)}
+        us = timed_graph(head, args.steps, args.warmup)
+        return {"profile_run": True, "point": point_key(*head), "us_mean": statistics.mean(us)}
 
-    # pre-warm (clocks settle), then the timed region of the headline M
+    # pre-warm (clocks settle), then the timed region of the headline point
     clock = ClockSampler(torch.cuda.current_device())
     t_end = time.time() + 0.5
     while time.time() < t_end:
-        timed_graph(args.M, 20, 0)
+        timed_graph(head, 5, 0)
     if dist is not None:
         dist.barrier()
     torch.cuda.synchronize()
     t0 = time.perf_counter()
-    us = timed_graph(args.M, args.steps, args.warmup)
+    us = timed_graph(head, args.steps, args.warmup)
     torch.cuda.synchronize()
     if dist is not None:
         dist.barrier()
@@ -363,19 +400,19 @@ def run_ours(args, rank, world):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
         us_mean = float(t.item())
 
-    work = layer_work(benches[args.M].case)
-    kern = per_kernel(args.M, max(10, min(args.steps, 50)))
+    work = layer_work(benches[head].case)
+    kern = per_kernel(head, max(10, min(args.steps, 50)))
     fc1_us = kern["fc1"]
-    hbm_peak = peaks["hbm_gbs"]
-    fp8_peak = fp8_peak_tflops(peaks)
     traffic = ncu_traffic(f"fc1_{args.workload}_M{args.M}")
-    if work["fc1_flops"] / (fp8_peak * 1e12) > work["fc1_bytes"] / (hbm_peak * 1e9):
+    sched = "block-scaled 128-row tiles" if (benches[head].sh.weight_fmt == synth.SCALE_UE8M0 and
+                                             benches[head].sh.act_fmt == synth.SCALE_UE8M0) else "FC1 schedule"
+    if work["fc1_flops"] / (fp8_tflops * 1e12) > work["fc1_bytes"] / (hbm_peak * 1e9):
         achieved = work["fc1_flops"] / (fc1_us * 1e-6) / 1e12
-        roofline = {"kernel": "fc1 (grouped GEMM + SwiGLU + requant)", "bound": "tensor",
-                    "achieved": achieved, "peak": fp8_peak, "unit": "TFLOP/s",
-                    "frac": achieved / fp8_peak, "traffic": traffic,
+        roofline = {"kernel": f"fc1 (grouped GEMM + SwiGLU + requant, {sched})", "bound": "tensor",
+                    "achieved": achieved, "peak": fp8_tflops, "unit": "TFLOP/s",
+                    "frac": achieved / fp8_tflops, "traffic": traffic,
                     "algorithmic_flops": work["fc1_flops"], "avg_launch_us": fc1_us,
-                    "peak_source": f"{peaks['source']}: 2 x MEASURED_PEAKS bf16_tflops (dense FP8 = 2x BF16)"}
+                    "peak_source": fp8_source}
     else:
         achieved = work["fc1_bytes"] / (fc1_us * 1e-6) / 1e9
         roofline = {"kernel": "fc1 (grouped GEMM + SwiGLU + requant)", "bound": "hbm",
@@ -384,9 +421,9 @@ def run_ours(args, rank, world):
                     "algorithmic_bytes": work["fc1_bytes"], "avg_launch_us": fc1_us,
                     "peak_source": f"{peaks['source']} (MEASURED_PEAKS hbm_gbs)"}
 
-    def layer_roof(M, t_us):
-        w = layer_work(benches[M].case)
-        t_f = w["flops"] / (fp8_peak_tflops(peaks) * 1e12)
+    def layer_roof(pt, t_us):
+        w = layer_work(benches[pt].case)
+        t_f = w["flops"] / (fp8_tflops * 1e12)
         t_b = w["layer_bytes"] / (hbm_peak * 1e9)
         return {"us": t_us, "roofline_us": max(t_f, t_b) * 1e6,
                 "frac_of_roofline": max(t_f, t_b) * 1e6 / t_us,
@@ -396,42 +433,86 @@ def run_ours(args, rank, world):
                 "occupied_experts": w["occupied_experts"]}
 
     sweep_out = {}
-    for M in sweep:
-        steps_us = us if M == args.M else timed_graph(M, max(20, args.steps // 2), 3)
-        t_us = us_mean if M == args.M else statistics.mean(steps_us)
-        sweep_out[str(M)] = layer_roof(M, t_us)
-        sweep_out[str(M)]["p50_us"] = statistics.median(steps_us)
-        sweep_out[str(M)]["per_kernel_us"] = kern if M == args.M else per_kernel(M, 20)
+    for pt in points:
+        steps_us = us if pt == head else timed_graph(pt, max(20, args.steps // 2), 3)
+        t_us = us_mean if pt == head else statistics.mean(steps_us)
+        key = point_key(*pt)
+        sweep_out[key] = layer_roof(pt, t_us)
+        sweep_out[key]["p50_us"] = statistics.median(steps_us)
+        sweep_out[key]["per_kernel_us"] = kern if pt == head else per_kernel(pt, 20)
 
-    e2e_us, h2d, d2h = e2e(args.M, max(10, min(args.steps, 100)), 3)
+    e2e_us, h2d, d2h = e2e(head, max(10, min(args.steps, 100)), 3)
 
+    shape = synth.SHAPES[args.workload]
     line = {
         "metric": METRIC, "value": us_mean, "unit": "us", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": us_mean / 1e3, "higher_is_better": False,
         "p50_us": statistics.median(us),
         "scaling": "weak", "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-        "config": {"workload": workload_name(shape, args.M, args.n),
-                   "clamp": ("none" if shape.clamp_mode == 0 else
-                             f"SwiGLU clamp {shape.limit} {'before' if shape.clamp_mode == 1 else 'after'} SiLU"),
-                   "scales": f"weights {FMT_NAMES[shape.weight_fmt]} 128x128, activations {FMT_NAMES[shape.act_fmt]} 1x128",
-                   "l2": "flushed before every step (512 MB write)", "timing": "CUDA graph replay, CUDA events",
-                   "parallelism": f"replicas x{world}"},
+        "config": bench_config(shape, args.M, args.n, world),
         "roofline": roofline,
-        "layer_roofline": sweep_out[str(args.M)],
+        "layer_roofline": sweep_out[point_key(*head)],
+        "fp8_peak_tflops": fp8_tflops, "fp8_peak_source": fp8_source,
         "sweep": sweep_out,
         "e2e": {"value": e2e_us, "unit": "us", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "api": "MoELayer.__call__ (C ABI moe_fp8_block_forward); x, ids and routing "
                        "weights copied in from one pinned staging buffer, the output copied back "
                        "to pinned memory"},
-        "gpu_launches": launches_per_forward(benches[args.M].case) * args.steps,
+        "gpu_launches": launches_per_forward(benches[head].case) * args.steps,
         "clocks": clocks,
         "timed_wall_s": wall,
     }
     if rank == 0 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(benches[args.M].case)
+        line["cpu_baseline"] = cpu_baseline(benches[head].case)
     if dist is not None:
         dist.destroy_process_group()
     return line
+
+
+# ------------------------------------------------------------ FP8 peak
+def measure_peaks():
+    """Dense FP8 GEMM throughput of this part: torch._scaled_mm (cuBLASLt) on e4m3 8192^3 with
+    per-tensor scales and a BF16 output, best of 10 (burst) and back to back for 4 s (sustained), with
+    the SM clocks sampled meanwhile."""
+    import torch
+    n = 8192
+    flops = 2.0 * n ** 3
+    a = (torch.randn(n, n, device="cuda") * 0.5).to(torch.float8_e4m3fn)
+    b = (torch.randn(n, n, device="cuda") * 0.5).to(torch.float8_e4m3fn).t()   # column-major
+    one = torch.ones((), device="cuda", dtype=torch.float32)
+
+    def mm():
+        return torch._scaled_mm(a, b, scale_a=one, scale_b=one, out_dtype=torch.bfloat16)
+
+    for _ in range(5):
+        mm()
+    torch.cuda.synchronize()
+    clock = ClockSampler(torch.cuda.current_device())
+    best = float("inf")
+    for _ in range(10):
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        mm()
+        e1.record()
+        e1.synchronize()
+        best = min(best, e0.elapsed_time(e1) * 1e-3)
+    t_end = time.time() + 4.0
+    reps, e0 = 0, torch.cuda.Event(enable_timing=True)
+    e0.record()
+    while time.time() < t_end:
+        for _ in range(20):
+            mm()
+        reps += 20
+        torch.cuda.synchronize()
+    e1 = torch.cuda.Event(enable_timing=True)
+    e1.record()
+    e1.synchronize()
+    sustained = flops * reps / (e0.elapsed_time(e1) * 1e-3) / 1e12
+    return {"fp8_tflops": flops / best / 1e12, "fp8_tflops_sustained": sustained,
+            "how": "torch._scaled_mm float8_e4m3fn 8192^3 (2 N^3 flops), per-tensor scales, bf16 out: "
+                   "best of 10 (burst); back to back for 4 s (sustained); CUDA events",
+            "torch": torch.__version__, "gpu": torch.cuda.get_device_name(),
+            "clocks": clock.stop()}
 
 
 # ---------------------------------------------------------- the oracle arm
@@ -473,8 +554,9 @@ def cpu_baseline(case: synth.LayerCase, budget_s: float = 12.0):
 
 
 def reference_arm(args):
-    weights = synth.make_weights(synth.SHAPES[WORKLOAD])
-    case = synth.make_case(WORKLOAD, args.M, seed=2000 + args.M, weights=weights)
+    shape = synth.SHAPES[args.workload]
+    weights = synth.make_weights(shape)
+    case = synth.make_case(args.workload, args.M, args.n, seed=2000 + args.M, weights=weights)
     per_step = []
     for _ in range(args.warmup + args.steps):
         sec_tok, _ = time_oracle(case, 0.0, max_tokens=1)
@@ -485,9 +567,10 @@ def reference_arm(args):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": us_layer / 1e3, "higher_is_better": False, "scaling": "weak",
         "vs_baseline": None, "dtype": "fp8_e4m3", "data": "synthetic",
-        "config": {"workload": f"decode MoE layer E=288 H=4096 I=512 top-8 M={args.M}"},
+        "config": bench_config(shape, args.M, args.n, 1),
         "cpu_baseline": {"value": us_layer, "unit": "us", "cores": cpu_cores(), "kind": "oracle",
-                         "sample": f"per step: 1 token of the M={args.M} layer, time x {case.n}"},
+                         "sample": f"per step: 1 of the {case.n} live tokens of the same layer through "
+                                   f"the oracle, time x {case.n}"},
         "e2e": {"value": us_layer, "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -499,16 +582,19 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.SHAPES),
-                    help="layer shape (default: the decode layer the metric is quoted on)")
+                    help="layer shape (default: the padded layer E=32 H=7168 I=2048)")
     ap.add_argument("--M", type=int, default=None, help="token capacity of the headline point")
     ap.add_argument("--n", type=int, default=None,
                     help="live tokens at --M (default: the workload's live count for M, else M)")
     ap.add_argument("--no-sweep", action="store_true")
     ap.add_argument("--sweep", action="store_true",
-                    help="also measure every M of the workload's sweep (the decode workload always does)")
+                    help="measure every point of --workload's sweep (default: the fixed list of "
+                         "points beside the default workload)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-run", action="store_true",
                     help="only W + K graph replays of the headline point (for ncu captures)")
+    ap.add_argument("--measure-peaks", action="store_true",
+                    help="time the dense FP8 GEMM peak and print it as JSON")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)
     if args.M is None:
@@ -517,6 +603,9 @@ def main():
         args.n = dict(synth.SWEEPS.get(args.workload, [])).get(args.M, args.M)
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
+    if args.measure_peaks:
+        print(json.dumps(measure_peaks()), flush=True)
+        return 0
     if args.impl == "reference":
         if rank == 0:
             print(json.dumps(reference_arm(args)), flush=True)

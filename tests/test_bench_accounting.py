@@ -42,3 +42,23 @@ def test_layer_work_counts_live_pairs_and_occupied_experts():
     assert w["fc1_flops"] == 4.0 * w["pairs"] * sh.H * sh.I
     per_expert = 3 * sh.H * sh.I + 4 * ((2 * sh.I // 128) * (sh.H // 128) + (sh.H // 128) * (sh.I // 128))
     assert w["layer_bytes"] == w["occupied_experts"] * per_expert + 4 * 5 * sh.H + 8 * 5 * sh.topk
+
+
+def test_default_headline_is_the_largest_layer_and_sweep_keeps_decode():
+    shape = synth.SHAPES[bench.WORKLOAD]
+    assert (shape.E, shape.H, shape.I, shape.topk) == (32, 7168, 2048, 8)
+    assert shape.weight_fmt == shape.act_fmt == synth.SCALE_UE8M0
+    pts = set(bench.SWEEP_POINTS)
+    assert {("decode", 1, 1), ("decode", 4, 4), ("decode", 32, 32), ("padded", 512, 16),
+            ("padded_fp32", 4096, 4096)} <= pts
+    cfg = bench.bench_config(shape, 4096, 4096, 1)
+    assert cfg["workload"] == "padded MoE layer E=32 H=7168 I=2048 top-8 M=4096"
+
+
+def test_reference_arm_reports_the_same_config():
+    args = types.SimpleNamespace(workload="tiny", M=16, n=16, steps=1, warmup=1, gpus=1)
+    line = bench.reference_arm(args)
+    assert line["impl"] == "reference"
+    assert line["config"] == bench.bench_config(synth.SHAPES["tiny"], 16, 16, 1)
+    assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0
