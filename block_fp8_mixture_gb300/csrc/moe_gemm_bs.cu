@@ -324,8 +324,12 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       if (kFC1) {
         fc1_item_epilogue(p, w, acc, row, wg, rlive, red);
       } else {
-        fc2_item_epilogue(p, w, acc, row, wg, q, lane, qlive, rlive, ystage + ew * TC::YWarpBytes,
-                          &tmY, &tmY3);
+        if (TC::YByGroup)
+          fc2_item_epilogue_by_group(p, w, acc, row, wg, q, lane, qlive, rlive,
+                                     ystage + ew * TC::YWarpBytes, &tmY);
+        else
+          fc2_item_epilogue(p, w, acc, row, wg, q, lane, qlive, rlive, ystage + ew * TC::YWarpBytes,
+                            &tmY, &tmY3);
       }
     }
   }

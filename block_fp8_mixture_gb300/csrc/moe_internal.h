@@ -61,7 +61,10 @@ constexpr int kMaxPK = 2;
 template <bool kFC1, bool kBS = false>
 struct TileCfg {
   static constexpr int PK = (kFC1 && !kBS) ? 2 : 1;
-  static constexpr int Stages = kFC1 ? (kBS ? 4 : 2) : 3;
+  // FC2 of the block-scaled kernel stores its output one 8-row group at a time through 2 KB per warp,
+  // which leaves room for a fourth operand stage
+  static constexpr bool YByGroup = !kFC1 && kBS;
+  static constexpr int Stages = kFC1 ? (kBS ? 4 : 2) : (YByGroup ? 4 : 3);
   static constexpr int ABytes = kBM * kBK * PK;
   static constexpr int BHalf = kGroup * kBK * PK;     // 128 weight rows
   static constexpr int StageBytes = ABytes + 2 * BHalf;
@@ -70,7 +73,8 @@ struct TileCfg {
   // scale slots form their own ring, deeper than the operand ring: an operand stage is released
   // as soon as the MMAs have read it, while the promotion warps still read the stage's scales
   static constexpr int ScaleSlots = Stages + 2;
-  static constexpr int YWarpBytes = kFC1 ? 0 : 8192;  // 32 rows x 128 BF16 columns per warp
+  // 32 rows x 128 BF16 columns per warp, or 8 rows with YByGroup
+  static constexpr int YWarpBytes = kFC1 ? 0 : (YByGroup ? 2048 : 8192);
   static constexpr int Smem = Stages * StageBytes + ScaleSlots * SlotBytes + 8 * YWarpBytes +
                               1024 /*align*/ + 1024 /*bars*/ + 2 * kBM * 4 /*row amax*/;
 };

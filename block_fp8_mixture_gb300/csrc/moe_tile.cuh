@@ -198,4 +198,55 @@ __device__ __forceinline__ void fc2_item_epilogue(const GemmParams& p, const Ite
   }
 }
 
+// FC2 with a 2 KB staging buffer per warp: the same BF16 stores as fc2_item_epilogue, one 8-row group
+// at a time.  For each fully live group of this warp (rows 32*g + 8*q .. +7, in increasing g), the
+// group's eight lanes write their rows into `buf` as two 128-byte-swizzled 8 x 64 boxes and lane 0
+// issues two 2-D stores; the buffer is reused for the next group once the stores have read it.
+// Rows of a partly live group are written from registers.  The small buffer leaves shared memory for
+// a fourth operand stage.
+__device__ __forceinline__ void fc2_item_epilogue_by_group(const GemmParams& p, const Item& w,
+                                                           const float* acc, int row, int wg, int q,
+                                                           int lane, bool qlive, bool rlive,
+                                                           uint8_t* buf, const CUtensorMap* tmY) {
+  const int col0 = w.nb * kBN + wg * kGroup;
+  if (!qlive || col0 >= p.out_cols) return;
+  const uint32_t buf_s = smem_addr(buf);
+  const int t = lane & 7;
+  const int g_mine = lane >> 3;
+  if (32 * g_mine + 8 * q + 8 > w.live && rlive) {
+    uint16_t* dst = p.y + (size_t)(w.m0 + row) * p.out_cols + col0;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const float* v = acc + c * 8;
+      *reinterpret_cast<uint4*>(dst + c * 8) =
+          make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                     pack_bf16x2(v[6], v[7]));
+    }
+  }
+#pragma unroll 1
+  for (int g = 0; g < 4; ++g) {
+    const int grow = 32 * g + 8 * q;
+    if (grow + 8 > w.live) break;            // later groups of this warp are not fully live either
+    if (lane == 0) bulk_wait_group_read0();  // the previous stores have read the buffer
+    __syncwarp();
+    if (g_mine == g) {
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const float* v = acc + c * 8;
+        const int half = c >> 3, cc = c & 7;
+        *reinterpret_cast<uint4*>(buf + half * 1024 + t * 128 + ((cc ^ t) << 4)) =
+            make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                       pack_bf16x2(v[6], v[7]));
+      }
+      fence_proxy_async_smem();
+    }
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmY, col0, w.m0 + grow, buf_s);
+      tma_store_2d(tmY, col0 + 64, w.m0 + grow, buf_s + 1024);
+      bulk_commit_group();
+    }
+  }
+}
+
 }  // namespace moe
