@@ -68,20 +68,6 @@ __device__ __forceinline__ Chunk decode_chunk(const GemmParams& p, int item) {
   return c;
 }
 
-__device__ __forceinline__ float s_swiglu(float g, float u, int mode, float lim) {
-  if (mode == MOE_CLAMP_BEFORE_SILU) {
-    g = fminf(g, lim);
-    u = fminf(fmaxf(u, -lim), lim);
-  }
-  const float sig = __frcp_rn(__fadd_rn(1.0f, expf(-g)));   // correctly rounded 1/(1+e^-g)
-  float silu = __fmul_rn(g, sig);
-  if (mode == MOE_CLAMP_AFTER_SILU) {
-    silu = fminf(silu, lim);
-    u = fminf(fmaxf(u, -lim), lim);
-  }
-  return __fmul_rn(silu, u);
-}
-
 __device__ __forceinline__ void s_drain_wait(uint32_t bar, uint32_t parity, int* status) {
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(bar, parity)) {
@@ -433,7 +419,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
 #pragma unroll 1
         for (int c = 0; c < trips; ++c) {
           if (c < ntok) {
-            float h = s_swiglu(bf16_round(acc0[0]), bf16_round(acc1[0]), p.clamp_mode,
+            float h = swiglu(bf16_round(acc0[0]), bf16_round(acc1[0]), p.clamp_mode,
                                p.clamp_limit);
             if (p.numerics == MOE_NUMERICS_RECIPROCAL) h = bf16_round(h);
             acc0[0] = h;
