@@ -69,8 +69,21 @@ cudaError_t launch_quant(const QuantParams& p, cudaStream_t s) {
 // fp32 in the top-k sum, not the FC2 accumulators.)
 // out[t, c] = bf16( sum_j RN(RN(w[t,j] * y[row_j, c]) ) ) over pairs j with a row, j ascending
 // (the fp32 sum itself when out_fp32: an expert-parallel rank's partial output).
-// Each thread produces 8 consecutive columns (16-byte loads of y and a 16-byte store).
+// Each thread produces 8 consecutive columns (16-byte loads of y and a 16-byte store).  The token's
+// pair rows and routing weights are read first, then the y loads go out four at a time, so a
+// token costs two or three dependent memory round trips instead of one per pair; the sum itself
+// still runs over j in ascending order.
 constexpr int kReduceThreads = 128;
+constexpr int kReduceBatch = 4;
+
+__device__ __forceinline__ void reduce_add8(float* acc, const uint4& raw, float w) {
+  const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, bf16_bits_to_f32(u[i] & 0xFFFFu)));
+    acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, bf16_bits_to_f32(u[i] >> 16)));
+  }
+}
 
 __global__ void __launch_bounds__(kReduceThreads) k_topk_reduce(ReduceParams p) {
   const long t = blockIdx.x;
@@ -81,20 +94,28 @@ __global__ void __launch_bounds__(kReduceThreads) k_topk_reduce(ReduceParams p) 
   if (t >= n) return;
   const int c0 = (blockIdx.y * kReduceThreads + threadIdx.x) * 8;
   if (c0 >= p.H) return;
+  const int topk = p.topk;
+  int rows[kMaxTopk];
+  float wts[kMaxTopk];
+#pragma unroll
+  for (int j = 0; j < kMaxTopk; ++j) {
+    rows[j] = j < topk ? p.pair_row[t * topk + j] : -1;
+    wts[j] = j < topk ? p.topk_weights[t * topk + j] : 0.0f;
+  }
   float acc[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
-  for (int j = 0; j < p.topk; ++j) {
-    const int row = p.pair_row[t * p.topk + j];
-    if (row < 0) continue;
-    const float w = p.topk_weights[t * p.topk + j];
-    const uint4 raw = *reinterpret_cast<const uint4*>(p.y + (size_t)row * p.H + c0);
-    const uint32_t u[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      acc[2 * i] = __fadd_rn(acc[2 * i], __fmul_rn(w, bf16_bits_to_f32(u[i] & 0xFFFFu)));
-      acc[2 * i + 1] = __fadd_rn(acc[2 * i + 1], __fmul_rn(w, bf16_bits_to_f32(u[i] >> 16)));
-    }
+  for (int j0 = 0; j0 < kMaxTopk; j0 += kReduceBatch) {
+    if (j0 >= topk) break;
+    uint4 raw[kReduceBatch];
+#pragma unroll
+    for (int u = 0; u < kReduceBatch; ++u)
+      if (rows[j0 + u] >= 0)
+        raw[u] = __ldg(reinterpret_cast<const uint4*>(p.y + (size_t)rows[j0 + u] * p.H + c0));
+#pragma unroll
+    for (int u = 0; u < kReduceBatch; ++u)
+      if (rows[j0 + u] >= 0) reduce_add8(acc, raw[u], wts[j0 + u]);
   }
   if (p.out_fp32) {
     float* o = static_cast<float*>(p.out) + t * p.H + c0;
