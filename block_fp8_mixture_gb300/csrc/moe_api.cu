@@ -81,7 +81,11 @@ moe_status make_plan(int M_cap, int E, int H, int I, int topk, int act_fmt, Plan
   // on the BF16 FC1 outputs (UE8M0 layers keep it in the block-scaled GEMM's overlapped epilogue)
   w.g1 = (!w.small_batch && act_fmt != MOE_SCALE_UE8M0) ? take((size_t)R_cap * 2 * I * 2) : 0;
   w.splitk_partial = take(w.fc1_ksplit > 1 ? (size_t)w.fc1_ksplit * P_cap * 2 * I * 4 : 0);
-  w.splitk_count = take(w.fc1_ksplit > 1 ? (size_t)w.C_cap * (I / kGroup) * 4 : 0);
+  // int32 counters: per (chunk, column block) split arrivals of the split-K FC1, or per row tile the
+  // FC1 items done, which the block-scaled FC2 waits on instead of the whole FC1 grid (tile schedule
+  // with UE8M0 activation scales)
+  w.splitk_count = take(w.fc1_ksplit > 1 ? (size_t)w.C_cap * (I / kGroup) * 4
+                        : (!w.small_batch && act_fmt == MOE_SCALE_UE8M0) ? (size_t)w.T_cap * 4 : 0);
   w.total_bytes = off;
   plan->M_cap = M_cap;
   plan->E = E;
@@ -307,7 +311,8 @@ static moe_status run_align(const int32_t* ids, const int32_t* d_n, int expert_o
   p.num_tiles = at<int32_t>(ws, pl.ws.num_tiles);
   p.status = at<int32_t>(ws, pl.ws.status);
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
-  p.splitk_count_len = pl.ws.fc1_ksplit > 1 ? pl.ws.C_cap * (pl.I / kGroup) : 0;
+  p.splitk_count_len = pl.ws.fc1_ksplit > 1 ? pl.ws.C_cap * (pl.I / kGroup)
+                       : (!pl.ws.small_batch && pl.act_fmt == MOE_SCALE_UE8M0) ? pl.ws.T_cap : 0;
   p.chunk_row0 = at<int32_t>(ws, pl.ws.chunk_row0);
   p.num_chunks = at<int32_t>(ws, pl.ws.num_chunks);
   p.cta_hist = at<int32_t>(ws, pl.ws.align_hist);
@@ -386,6 +391,9 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   p.splitk_partial = at<float>(ws, pl.ws.splitk_partial);
   p.splitk_count = at<int32_t>(ws, pl.ws.splitk_count);
   if (!small && p.ksplit != 1) return MOE_ERR_UNSUPPORTED_SHAPE;   // the tile kernels do not split K
+  // routed block-scaled layers: FC1 counts its finished items per row tile for FC2 (the alignment
+  // reset the counters); the batched layout keeps the grid-wide dependency
+  if (!small && bs && tile_row0 == nullptr) p.tile_ready = at<int32_t>(ws, pl.ws.splitk_count);
   const long items = (long)(small ? pl.ws.C_cap : pl.ws.T_cap) * p.n_blocks * p.ksplit;
   const int grid = (int)std::max(1L, std::min<long>(sm_count(), items));
   // tile schedule with fp32 activation scales: BF16 FC1 outputs, then SwiGLU + requant kernel
@@ -452,6 +460,10 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
                  !make_map_bf16_store3(&tmY3, y, pl.H, pl.ws.R_cap)))
     return MOE_ERR_CUDA;
   const bool bs = w_ue && pl.act_fmt == MOE_SCALE_UE8M0;   // scales applied inside the MMA
+  if (!small && bs && tile_row0 == nullptr) {
+    p.tile_ready = at<int32_t>(ws, pl.ws.splitk_count);   // FC1 items done per row tile
+    p.fc1_items_per_tile = pl.I / kGroup;
+  }
   const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
                           : bs  ? launch_fc2_bs(tmA, tmB, tmAS, tmS, tmY, tmY3, p, grid, s)
                                 : launch_fc2(tmA, tmB, tmAS, tmS, tmY, tmY3, p, grid, s);

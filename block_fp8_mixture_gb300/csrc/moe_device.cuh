@@ -102,6 +102,35 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
   return mbar_wait_limit(bar, parity, abort_flag, status, kWaitLimitNs);
 }
 
+// Bounded wait until the int32 at `counter` reaches `target` (acquire at GPU scope), for counters
+// other CTAs release; on expiry it raises the CTA abort flag and records MOE_ERR_DEVICE_TIMEOUT.
+__device__ __forceinline__ bool wait_counter_at_least(const int32_t* counter, int target,
+                                                      volatile int* abort_flag, int* status) {
+  auto load = [&] {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(counter) : "memory");
+    return v;
+  };
+  if (load() >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    __nanosleep(64);
+    if (load() >= target) return true;
+    if (*abort_flag) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      *abort_flag = 1;
+      atomicCAS(status, 0, (int)MOE_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Order this thread's acquire of data written by other CTAs through the generic proxy before its
+// later async-proxy (TMA) reads of global memory.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
 // ---------------------------------------------------------------------- TMA
 // 2-D tiled bulk tensor load into shared memory, completion counted on `bar` in bytes.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,

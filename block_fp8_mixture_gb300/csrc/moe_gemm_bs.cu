@@ -115,7 +115,10 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  grid_dep_wait();                 // the previous kernel's outputs are complete from here on
+  // FC2 with per-tile FC1 counters does not wait for the FC1 grid: its producer waits per row tile
+  // below.  The routing metadata it reads was complete before FC1's CTAs passed their own
+  // dependency wait, which precedes this launch.
+  if (kFC1 || p.tile_ready == nullptr) grid_dep_wait();
   grid_dep_launch_dependents();
 
   const int num_tiles = *p.num_tiles;
@@ -133,9 +136,20 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       // ---------------------------------------------------------- producer
       int sc = 0;
       bool ok = true;
+      int ready_tile = -1;
       const uint64_t pol_once = policy_evict_first();
-        for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
+      for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
         const Item w = decode_item(p, item);
+        if (!kFC1 && p.tile_ready != nullptr && w.tile != ready_tile) {
+          // every FC1 item of this row tile has written its FC2 input rows and scales
+          if (!wait_counter_at_least(p.tile_ready + w.tile, p.fc1_items_per_tile, abort_flag,
+                                     status)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_global();
+          ready_tile = w.tile;
+        }
         const bool shared = expert_weights_shared(p, w, num_tiles);
         const int brow0 = kFC1 ? w.e * p.b_rows_per_expert + w.nb * kGroup
                                : w.e * p.b_rows_per_expert + w.nb * kBN;
@@ -323,6 +337,15 @@ __global__ void __launch_bounds__(kBsThreads, 1)
       if (lane == 0) mbar_arrive(tempty_bar);     // the next item's MMAs may overwrite it
       if (kFC1) {
         fc1_item_epilogue(p, w, acc, row, wg, rlive, red);
+        if (p.tile_ready != nullptr) {
+          // the item's FC2 input rows are written: count it for its row tile (release at GPU scope
+          // after all 256 epilogue threads' stores)
+          named_barrier_sync(1, kTileEpiThreadsBar);
+          if (ew == 0 && lane == 0) {
+            __threadfence();
+            atomicAdd(p.tile_ready + w.tile, 1);
+          }
+        }
       } else {
         if (TC::YByGroup)
           fc2_item_epilogue_by_group(p, w, acc, row, wg, q, lane, qlive, rlive,

@@ -183,6 +183,11 @@ struct GemmParams {
   // tile schedule, fp32 activation scales: FC1 writes BF16 (gate | up) rows here instead of
   // running SwiGLU + requantization in its epilogue (nullptr: fused epilogue)
   uint16_t* g1;
+  // block-scaled tile schedule of a routed layer: FC1 adds one per finished item of row tile t to
+  // tile_ready[t]; FC2 starts a tile once fc1_items_per_tile items are in, instead of waiting for
+  // the whole FC1 grid (nullptr: FC2 waits for the previous kernel)
+  int32_t* tile_ready;
+  int fc1_items_per_tile;
 };
 
 // SwiGLU + 1x128 requantization of the BF16 FC1 outputs of live workspace rows.
