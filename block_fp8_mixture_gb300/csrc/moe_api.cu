@@ -422,8 +422,13 @@ static moe_status run_fc1(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+// after_fc1: the kernel launched just before this one on the stream is this layer's FC1 (the
+// whole-layer forward), so the block-scaled FC2 may rely on the per-tile FC1 counters alone and skip
+// the wait for the previous grid; otherwise (the standalone FC2 step) it waits for the previous
+// grid and checks the counters as well.
 static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaStream_t s,
-                          const int32_t* tile_row0 = nullptr, void* y_target = nullptr) {
+                          const int32_t* tile_row0 = nullptr, void* y_target = nullptr,
+                          bool after_fc1 = false) {
   if (pl.ws.R_cap == 0) return MOE_OK;
   CUtensorMap tmA, tmB, tmAS, tmS;
   const bool w_ue = a->weight_scale_fmt == MOE_SCALE_UE8M0;
@@ -463,6 +468,7 @@ static moe_status run_fc2(const moe_fwd_args* a, const Plan& pl, void* ws, cudaS
   if (!small && bs && tile_row0 == nullptr) {
     p.tile_ready = at<int32_t>(ws, pl.ws.splitk_count);   // FC1 items done per row tile
     p.fc1_items_per_tile = pl.I / kGroup;
+    p.wait_prev_grid = after_fc1 ? 0 : 1;
   }
   const cudaError_t err = small ? launch_fc2_small(tmA, tmB, tmS, p, grid, s)
                           : bs  ? launch_fc2_bs(tmA, tmB, tmAS, tmS, tmY, tmY3, p, grid, s)
@@ -619,7 +625,8 @@ moe_status moe_fp8_block_forward(const moe_fwd_args* args, void* workspace, size
   if ((st = run_quant(args->x, args->d_num_tokens, pl, args->numerics, workspace, s)) != MOE_OK)
     return st;
   if ((st = run_fc1(args, pl, workspace, s)) != MOE_OK) return st;
-  if ((st = run_fc2(args, pl, workspace, s)) != MOE_OK) return st;
+  if ((st = run_fc2(args, pl, workspace, s, nullptr, nullptr, /*after_fc1=*/true)) != MOE_OK)
+    return st;
   return run_reduce(args, pl, workspace, s);
 }
 

@@ -115,10 +115,11 @@ __global__ void __launch_bounds__(kBsThreads, 1)
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_slot;
-  // FC2 with per-tile FC1 counters does not wait for the FC1 grid: its producer waits per row tile
-  // below.  The routing metadata it reads was complete before FC1's CTAs passed their own
-  // dependency wait, which precedes this launch.
-  if (kFC1 || p.tile_ready == nullptr) grid_dep_wait();
+  // Inside the whole-layer forward, FC2 with per-tile FC1 counters does not wait for the FC1 grid:
+  // its producer waits per row tile below.  The routing metadata it reads was complete before FC1's
+  // CTAs passed their own dependency wait, which precedes this launch (FC1 is the kernel launched
+  // just before).  The standalone FC2 step waits for the previous grid as well.
+  if (kFC1 || p.tile_ready == nullptr || p.wait_prev_grid) grid_dep_wait();
   grid_dep_launch_dependents();
 
   const int num_tiles = *p.num_tiles;

@@ -184,10 +184,12 @@ struct GemmParams {
   // running SwiGLU + requantization in its epilogue (nullptr: fused epilogue)
   uint16_t* g1;
   // block-scaled tile schedule of a routed layer: FC1 adds one per finished item of row tile t to
-  // tile_ready[t]; FC2 starts a tile once fc1_items_per_tile items are in, instead of waiting for
-  // the whole FC1 grid (nullptr: FC2 waits for the previous kernel)
+  // tile_ready[t]; FC2 starts a tile once fc1_items_per_tile items are in.  Inside the whole-layer
+  // forward (FC1 launched just before FC2) that replaces FC2's wait for the FC1 grid (nullptr: FC2
+  // waits for the previous kernel only)
   int32_t* tile_ready;
   int fc1_items_per_tile;
+  int wait_prev_grid;       // with tile_ready: also wait for the previous grid (standalone FC2)
 };
 
 // SwiGLU + 1x128 requantization of the BF16 FC1 outputs of live workspace rows.

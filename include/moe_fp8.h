@@ -186,6 +186,11 @@ moe_status moe_fc1_swiglu_quant(const moe_fwd_args* args, void* workspace, size_
  * Routing weights are not applied here (TensorRT-LLM page, rounding-fix commit). */
 moe_status moe_fc2(const moe_fwd_args* args, void* workspace, size_t workspace_bytes,
                    moe_stream_t stream);
+/*   For routed layers on the 128-row tiles with UE8M0 weight and activation scales, FC2 also checks,
+ *   per row tile, that moe_fc1_swiglu_quant has run since the last moe_align (FC1 counts its
+ *   finished items per tile; inside moe_fp8_block_forward those counts let FC2 start on finished
+ *   tiles before the FC1 grid ends).  Called without that FC1, its bounded wait runs out after 1 s
+ *   and the status word reads MOE_ERR_DEVICE_TIMEOUT. */
 
 /* Top-k weighted unpermute/sum: out[t] = bf16( sum_j fp32(w[t,j] * y[pair_row[t*k+j]]) ), j ascending,
  * fp32 multiply and add rounded separately, dropped pairs skipped; rows t < n only. */

@@ -444,6 +444,33 @@ def test_bounded_wait_expiry_reported_and_context_usable():
     assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
 
 
+def test_tile_ready_wait_expiry_reported_and_context_usable():
+    """The block-scaled FC2 of a routed layer waits, per row tile, for FC1's completion counters
+    instead of the whole FC1 grid.  Run right after the alignment reset those counters, with no FC1
+    in between, its bounded wait runs out (1 s), the status word reads MOE_ERR_DEVICE_TIMEOUT, and
+    the next forward on the same workspace runs normally and reproduces the earlier output."""
+    shape = synth.small_shape("tile_to", E=4, H=384, I=256, topk=2, act_fmt=2, weight_fmt=2)
+    case = synth.make_case("tile_to", 96, 80, shape=shape)
+    sh = case.shape
+    assert moe.workspace_plan(96, sh.E, sh.H, sh.I, sh.topk, sh.act_fmt)["small_batch"] == 0
+    dev = device_case(case)
+    o1, ws, _ = run_forward(case, dev)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    moe.align(dev["ids"], sh.E, sh.H, sh.I, ws, d_num_tokens=dev["n"], act_fmt=sh.act_fmt)
+    out = torch.empty((96, sh.H), dtype=torch.bfloat16, device="cuda")
+    args = moe.make_args(dev["x"], dev["ids"], dev["w"], dev["w13"], dev["s13"], dev["w2"], dev["s2"],
+                         out, E=sh.E, H=sh.H, I=sh.I, topk=sh.topk, M_cap=96, d_num_tokens=dev["n"],
+                         weight_fmt=sh.weight_fmt, act_fmt=sh.act_fmt)
+    moe.fc2(args, ws)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == moe.MOE_ERR_DEVICE_TIMEOUT
+    o2, _, _ = run_forward(case, dev, ws=ws, poison=False)
+    torch.cuda.synchronize()
+    assert moe.last_device_status(ws) == moe.MOE_OK
+    assert torch.equal(o1[:80].view(torch.int16), o2[:80].view(torch.int16))
+
+
 def test_graph_replay_changing_routing():
     """Capture once, then change routing and the live-token count in place between replays."""
     shape = synth.small_shape("graph", E=16, H=512, I=256, topk=4)
