@@ -400,10 +400,12 @@ def test_deterministic():
 
 
 @pytest.mark.parametrize("name,M,n", [("decode", 1, 1), ("decode", 4, 4), ("decode", 32, 29),
-                                      ("mid", 128, 128), ("glm_slice", 1024, 1000)])
+                                      ("mid", 128, 128), ("glm_slice", 1024, 1000),
+                                      ("padded", 512, 16)])
 def test_step_entry_points_match_forward(name, M, n):
     """The five per-step entry points run back to back give the whole-layer forward's output bit for
-    bit (small-batch schedule for the decode and mid cases, 128-row tiles for glm_slice)."""
+    bit (small-batch schedule for the decode and mid cases, 128-row tiles for glm_slice, block-scaled
+    128-row tiles for padded, where the standalone FC2 also checks FC1's per-tile counters)."""
     case = synth.make_case(name, M, n)
     sh = case.shape
     dev = device_case(case)
@@ -505,13 +507,15 @@ def test_graph_replay_changing_routing():
         assert bool((out[n:].view(torch.int16) == -1).all())
 
 
-@pytest.mark.parametrize("world", [2, 3])
-def test_expert_parallel_virtual_ranks(world):
+@pytest.mark.parametrize("world,fmt", [(2, 0), (3, 0), (2, 2)])
+def test_expert_parallel_virtual_ranks(world, fmt):
     """Expert-parallel slices run one after another on one GPU ("virtual ranks"): each rank's fp32
     partial matches the oracle's partial, rows t >= n stay untouched, and the rank-ordered fp32 sum
-    rounded once to BF16 matches the whole layer."""
-    E, H, I, k, M, n = 16, 512, 256, 4, 64, 50
-    shape = synth.small_shape("ep_gpu", E=E, H=H, I=I, topk=k)
+    rounded once to BF16 matches the whole layer.  With UE8M0 scales and 256 pairs on 16 experts the
+    slices run the block-scaled 128-row tiles (FC2 starting on FC1's finished tiles)."""
+    E, H, I, k = 16, 512, 256, 4
+    M, n = (64, 50) if fmt == 0 else (256, 250)
+    shape = synth.small_shape("ep_gpu", E=E, H=H, I=I, topk=k, act_fmt=fmt, weight_fmt=fmt)
     case = synth.make_case("ep_gpu", M, n, shape=shape)
     dev = device_case(case)
     w = case.weights
@@ -520,18 +524,21 @@ def test_expert_parallel_virtual_ranks(world):
     for r in range(world):
         first, cnt = moe.expert_slice(E, world, r)
         sl = slice(first, first + cnt)
-        ws = moe.alloc_workspace(M, cnt, H, I, k)
+        if fmt == 2:
+            assert moe.workspace_plan(M, cnt, H, I, k, fmt)["small_batch"] == 0
+        ws = moe.alloc_workspace(M, cnt, H, I, k, fmt)
         out = torch.full((M, H), float("nan"), dtype=torch.float32, device="cuda")
         args = moe.make_args(dev["x"], dev["ids"], dev["w"], dev["w13"][sl], dev["s13"][sl],
                              dev["w2"][sl], dev["s2"][sl], out, E=cnt, H=H, I=I, topk=k, M_cap=M,
-                             d_num_tokens=dev["n"], expert_offset=first, out_fp32=True)
+                             d_num_tokens=dev["n"], expert_offset=first, out_fp32=True,
+                             weight_fmt=fmt, act_fmt=fmt)
         moe.forward(args, ws)
         torch.cuda.synchronize()
         assert moe.last_device_status(ws) == moe.MOE_OK
         part = out.cpu().numpy()
         ref = oracle.moe_forward(case.x, case.topk_ids, case.topk_weights, w.w13[sl], w.s13[sl],
                                  w.w2[sl], w.s2[sl], expert_offset=first, out_fp32=True,
-                                 tokens=np.arange(n))
+                                 tokens=np.arange(n), act_fmt=fmt, weight_fmt=fmt)
         assert np.all(np.isnan(part[n:]))
         assert np.abs(part[:n] - ref).max() <= 1e-2 * float(np.abs(whole).max())
         total += out.nan_to_num(0.0)
