@@ -418,6 +418,59 @@ def test_block_gemm_exact_integer_dot():
             assert acc[r, c] == exact_round_f32(Fraction(d, 2 ** 18))
 
 
+def _int_codes(codes):
+    """E4M3 codes as integers: value * 2^9 (every E4M3 value is an integer multiple of 2^-9)."""
+    return np.rint(fm.E4M3_VALUES[np.asarray(codes, np.uint8)] * 512).astype(np.int64)
+
+
+def _block_gemm_steps(aq, a_s, wq, w_s, accumulate="fused"):
+    """The per-128-K promotion evaluated in exact rationals: d = exact block dot, p = RN32(d),
+    sab = RN32(sa*sw), acc = RN32(acc + p*sab) with one rounding (a fused multiply-add; TensorRT-LLM
+    page, human review: the scale product is formed first).  `accumulate` selects a planted
+    variant: "separate" rounds p*sab before the add, "unrounded_sab" skips the scale-product
+    rounding."""
+    ia, iw = _int_codes(aq), _int_codes(wq)
+    R, K = aq.shape
+    N = wq.shape[0]
+    out = np.zeros((R, N), F32)
+    for r in range(R):
+        for c in range(N):
+            acc = Fraction(0)
+            for kb in range(K // 128):
+                sl = slice(kb * 128, (kb + 1) * 128)
+                d = Fraction(int(np.dot(ia[r, sl], iw[c, sl])), 2 ** 18)
+                p = Fraction(exact_round_f32(d))
+                sa, sw = Fraction(float(a_s[r, kb])), Fraction(float(w_s[c // 128, kb]))
+                if accumulate == "unrounded_sab":
+                    acc = Fraction(exact_round_f32(acc + p * sa * sw))
+                    continue
+                sab = Fraction(exact_round_f32(sa * sw))
+                if accumulate == "separate":
+                    acc = Fraction(exact_round_f32(acc + Fraction(exact_round_f32(p * sab))))
+                else:
+                    acc = Fraction(exact_round_f32(acc + p * sab))
+            out[r, c] = float(acc)
+    return out
+
+
+def test_block_gemm_promotion_step_by_step():
+    """Several K blocks with scales that are not powers of two: every output equals the stated
+    promotion sequence in exact rationals, and the two plausible misreadings (rounding p*sab before
+    the add; not rounding the scale product) each change some outputs."""
+    rng = np.random.default_rng(17)
+    R, N, K = 3, 256, 384
+    aq = fm.e4m3_encode(rng.standard_normal((R, K)).astype(F32) * 60)
+    wq = fm.e4m3_encode(rng.standard_normal((N, K)).astype(F32) * 60)
+    a_s = (rng.uniform(0.5, 1.0, (R, K // 128)) * 2.0 ** -9).astype(F32)
+    w_s = (rng.uniform(0.5, 1.0, (N // 128, K // 128)) * 2.0 ** -7).astype(F32)
+    got = oracle.block_gemm(aq, a_s, wq, w_s)
+    want = _block_gemm_steps(aq, a_s, wq, w_s)
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    for variant in ("separate", "unrounded_sab"):
+        bad = _block_gemm_steps(aq, a_s, wq, w_s, variant)
+        assert not np.array_equal(bad.view(np.uint32), want.view(np.uint32)), variant
+
+
 def test_block_gemm_vs_dequantized_matmul():
     rng = np.random.default_rng(11)
     R, N, K = 5, 256, 512
@@ -609,6 +662,49 @@ def test_topk_reduce_pin_catches_order_and_fused_accumulation():
 
     for planted in (descending, fused64):
         assert not np.array_equal(planted(y, w, present), want), planted.__name__
+
+
+def test_expert_rows_wiring_exact():
+    """One expert end to end (H = 256, I = 256, two rows), every step from its stated definition in
+    exact rationals: 1x128 quantization of x, the FC1 promotion, BF16 rounding of the gate/up sums,
+    the SwiGLU steps, requantization of h, the FC2 promotion and the final BF16 rounding.  Pins which
+    intermediate feeds which step (a dropped BF16 rounding of the FC1 sums, or gate and up swapped,
+    fails it)."""
+    rng = np.random.default_rng(23)
+    H = I = 256
+    x = fm.bf16_round(rng.standard_normal((2, H)).astype(F32))
+    w13 = fm.e4m3_encode(rng.standard_normal((2 * I, H)).astype(F32) * 100)
+    w2 = fm.e4m3_encode(rng.standard_normal((H, I)).astype(F32) * 100)
+    s13 = (rng.uniform(0.5, 1.0, (2 * I // 128, H // 128)) * 2.0 ** -8).astype(F32)
+    s2 = (rng.uniform(0.5, 1.0, (H // 128, I // 128)) * 2.0 ** -8).astype(F32)
+
+    def quant_rows(v):
+        q = np.zeros(v.shape, np.uint8)
+        sc = np.zeros((v.shape[0], v.shape[1] // 128), F32)
+        for r in range(v.shape[0]):
+            for g in range(v.shape[1] // 128):
+                grp = v[r, g * 128:(g + 1) * 128].tolist()
+                s = _expected_scale(max(abs(t) for t in grp), oracle.SCALE_FP32)
+                sc[r, g] = s
+                q[r, g * 128:(g + 1) * 128] = [_nearest_code(Fraction(t) / Fraction(s), t) for t in grp]
+        return q, sc
+
+    def run(round_g1=True, swap=False):
+        a1q, a1s = quant_rows(x)
+        g1 = _block_gemm_steps(a1q, a1s, w13, s13)
+        if round_g1:
+            g1 = fm.bf16_round(g1)
+        gate, up = (g1[:, I:], g1[:, :I]) if swap else (g1[:, :I], g1[:, I:])
+        h = np.array([[_swiglu_steps(float(gv), float(uv)) for gv, uv in zip(gr, ur)]
+                      for gr, ur in zip(gate, up)], F32)
+        a2q, a2s = quant_rows(h)
+        return fm.bf16_round(_block_gemm_steps(a2q, a2s, w2, s2))
+
+    got = oracle.expert_rows(x, w13, s13, w2, s2, oracle.SCALE_FP32, oracle.SCALE_FP32)
+    want = run()
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+    assert not np.array_equal(run(round_g1=False).view(np.uint32), want.view(np.uint32))
+    assert not np.array_equal(run(swap=True).view(np.uint32), want.view(np.uint32))
 
 
 # ----------------------------------------------------------- layer pins
