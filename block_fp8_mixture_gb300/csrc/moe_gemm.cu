@@ -20,8 +20,9 @@
 //                      completion, the promotion warps release the scale slot once they have
 //                      read it.  Rows of a tile past the expert's live end are loaded too (they
 //                      stay inside the workspace) and their results are discarded.
-//   warp 1 (one lane)  MMA issuer: 4 x 2 tcgen05.mma kind::f8f6f4 (M=128, N=128, K=32) per K
-//                      block into one of two 256-column fp32 accumulators in tensor memory.
+//   warp 1 (one lane)  MMA issuer: per K block 4 tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32;
+//                      4 x 2 with N=128 when a stage holds two K blocks) into one of two
+//                      256-column fp32 accumulators in tensor memory.
 //   warps 4..11        promotion + epilogue (224 registers after setmaxnreg).  A thread owns one
 //                      row and 128 of the 256 columns; per K block it reads its partial sums from
 //                      tensor memory (two loads in flight per wait) and accumulates
@@ -41,6 +42,9 @@
 namespace moe {
 
 constexpr uint32_t kIdesc = make_idesc_e4m3(kBM, kGroup);   // M = 128, N = 128 per MMA
+// M = 128, N = 256: one MMA per K step when the two weight halves are contiguous (one K block per
+// stage); about 520 cycles per 128x256x128 K block against about 770 for two N = 128 MMAs
+constexpr uint32_t kIdesc256 = make_idesc_e4m3(kBM, 2 * kGroup);
 
 // acc[0..63] += partial[t0 .. t0+31, t1 .. t1+31] * sab: both tensor-memory loads in flight before
 // the one wait, so a K block costs two load round trips instead of four.
@@ -229,8 +233,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           const uint64_t u_desc = make_sdesc_sw128(sB + kBHalfBytes + k * (kGroup * kBK));
 #pragma unroll
           for (int kk = 0; kk < kBK / 32; ++kk) {
-            mma_f8(d, adesc + 2 * kk, g_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
-            if (second) mma_f8(d + kGroup, adesc + 2 * kk, u_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+            if constexpr (kPK == 1) {
+              // both 128-row weight halves are contiguous: one N = 256 MMA per K step
+              mma_f8(d, adesc + 2 * kk, g_desc + 2 * kk, kIdesc256, kk > 0 ? 1u : 0u);
+            } else {
+              mma_f8(d, adesc + 2 * kk, g_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+              if (second) mma_f8(d + kGroup, adesc + 2 * kk, u_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
+            }
           }
           mma_commit(tfull_bar(b));
           ++c;
