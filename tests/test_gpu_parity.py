@@ -507,6 +507,45 @@ def test_graph_replay_changing_routing():
         assert bool((out[n:].view(torch.int16) == -1).all())
 
 
+def test_graph_replay_changing_routing_block_scaled_tiles():
+    """The block-scaled 128-row-tile schedule, whose FC2 starts on row tiles once FC1's per-tile
+    counters are complete: one captured forward replayed with new routing and live-token counts
+    (the alignment resets the counters on every replay) matches the oracle every time."""
+    E, H, I, k, M = 8, 512, 256, 4, 96
+    shape = synth.small_shape("graph_bs", E=E, H=H, I=I, topk=k, act_fmt=2, weight_fmt=2)
+    assert moe.workspace_plan(M, E, H, I, k, 2)["small_batch"] == 0
+    case = synth.make_case("graph_bs", M, M, shape=shape)
+    dev = device_case(case)
+    ws = moe.alloc_workspace(M, E, H, I, k, 2)
+    out = torch.empty((M, H), dtype=torch.bfloat16, device="cuda")
+    args = moe.make_args(dev["x"], dev["ids"], dev["w"], dev["w13"], dev["s13"], dev["w2"], dev["s2"],
+                         out, E=E, H=H, I=I, topk=k, M_cap=M, d_num_tokens=dev["n"], weight_fmt=2,
+                         act_fmt=2)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        moe.forward(args, ws, s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        moe.forward(args, ws, s)
+    rng = np.random.default_rng(78)
+    for n in (96, 41, 3, 96):
+        ids, w = synth.make_routing("softmax", M, E, k, rng)
+        case.topk_ids[:] = ids
+        case.topk_weights[:] = w
+        case.n = n
+        dev["ids"].copy_(torch.from_numpy(ids))
+        dev["w"].copy_(torch.from_numpy(w))
+        dev["n"].fill_(n)
+        out.view(torch.int16).fill_(-1)
+        g.replay()
+        torch.cuda.synchronize()
+        assert moe.last_device_status(ws) == moe.MOE_OK
+        gpu = bf16_tensor_to_f32(out)
+        assert_layer_close(gpu[:n], oracle_forward(case), f"block-scaled replay n={n}")
+        assert bool((out[n:].view(torch.int16) == -1).all())
+
+
 @pytest.mark.parametrize("world,fmt", [(2, 0), (3, 0), (2, 2)])
 def test_expert_parallel_virtual_ranks(world, fmt):
     """Expert-parallel slices run one after another on one GPU ("virtual ranks"): each rank's fp32
