@@ -140,7 +140,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
   const int kb_per_split = KB / p.ksplit;
   const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
   const int a_kb_bytes = a_ue ? kBM : kBM * 4;   // activation scales of one K block in a slot
-  const int w_per16 = b_ue ? 16 : 4;             // scale elements per 16 bytes
+  const int w_mask = b_ue ? 15 : 3;              // scale elements per 16 bytes, minus one
   int* status = p.status;
 
   const int nst_item = (kb_per_split + kPK - 1) / kPK;   // pipeline stages per work item
@@ -193,10 +193,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         // a 32-byte box from the 16-byte boundary at or below the stage's first block scale
         // holds the scales of all kPK K blocks
         const int i0 = sr0 * KB + kbs;
-        tma_load_1d(sS + kSlotW, &tmS, i0 - i0 % w_per16, sfull_bar(sl));
+        tma_load_1d(sS + kSlotW, &tmS, i0 & ~w_mask, sfull_bar(sl));
         if (has_sr1) {
           const int i1 = sr1 * KB + kbs;
-          tma_load_1d(sS + kSlotW + 128, &tmS, i1 - i1 % w_per16, sfull_bar(sl));
+          tma_load_1d(sS + kSlotW + 128, &tmS, i1 & ~w_mask, sfull_bar(sl));
         }
         ++sc;
       }
@@ -287,8 +287,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           if (qlive) {
             const float sa = smem_scale_at(slot + k * a_kb_bytes, row, a_ue);
             const int i0 = sr0 * KB + kbs, i1 = sr1 * KB + kbs;
-            const float sw0 = smem_scale_at(slot + kSlotW, i0 % w_per16 + k, b_ue);
-            const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotW + 128, i1 % w_per16 + k, b_ue)
+            const float sw0 = smem_scale_at(slot + kSlotW, (i0 & w_mask) + k, b_ue);
+            const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotW + 128, (i1 & w_mask) + k, b_ue)
                                       : 0.0f;
             sab0 = __fmul_rn(sa, sw0);
             sab1 = __fmul_rn(sa, sw1);

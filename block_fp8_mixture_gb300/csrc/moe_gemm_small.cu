@@ -181,7 +181,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int kb_per_split = KB / p.ksplit;
   const int a_ue = p.a_scale_ue8m0, b_ue = p.b_scale_ue8m0;
   const int a_scale_bytes = a_ue ? kSN : kSN * 4;
-  const int w_per16 = b_ue ? 16 : 4;
+  const int w_mask = b_ue ? 15 : 3;   // scale elements per 16 bytes, minus one
   const int ncb = p.b_rows_per_expert / kGroup;
   int* status = p.status;
 
@@ -235,10 +235,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
                                 ((size_t)kb * p.R_cap + w.row0) * (a_ue ? 1 : 4),
                         a_scale_bytes, sfull_bar(sl));
           const int i0 = sr0 * KB + kb;
-          tma_load_1d(sS + kSSlotW0, &tmS, i0 - i0 % w_per16, sfull_bar(sl));
+          tma_load_1d(sS + kSSlotW0, &tmS, i0 & ~w_mask, sfull_bar(sl));
           if (second) {
             const int i1 = sr1 * KB + kb;
-            tma_load_1d(sS + kSSlotW1, &tmS, i1 - i1 % w_per16, sfull_bar(sl));
+            tma_load_1d(sS + kSSlotW1, &tmS, i1 & ~w_mask, sfull_bar(sl));
           }
           ++it;
         }
@@ -326,8 +326,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
         if (ntok > 0) {
           const uint8_t* slot = slots + sl * kSSlotBytes;
           const int i0 = sr0 * KB + kb, i1 = sr1 * KB + kb;
-          const float sw0 = smem_scale_at(slot + kSSlotW0, i0 % w_per16, b_ue);
-          const float sw1 = has1 ? smem_scale_at(slot + kSSlotW1, i1 % w_per16, b_ue) : 0.0f;
+          const float sw0 = smem_scale_at(slot + kSSlotW0, (i0 & w_mask), b_ue);
+          const float sw1 = has1 ? smem_scale_at(slot + kSSlotW1, (i1 & w_mask), b_ue) : 0.0f;
           uint32_t r0[16], r1[16];
           const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kSBufCols + hb;
           tmem_ld16(t0, r0);
