@@ -278,8 +278,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint8_t* slot = slots + sl * kScaleSlotBytes;
         for (int k = 0; k < nv; ++k) {
           const int b = c & 1;
-          if (!mbar_wait(tfull_bar(b), (c >> 1) & 1, abort_flag, status) ||
-              (k == 0 && !mbar_wait(sfull_bar(sl), (sc / kSlots) & 1, abort_flag, status))) {
+          // the scales need only their slot: read them before waiting for the partial sums
+          if (k == 0 && !mbar_wait(sfull_bar(sl), (sc / kSlots) & 1, abort_flag, status)) {
             ok = false;
             break;
           }
@@ -292,6 +292,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                                       : 0.0f;
             sab0 = __fmul_rn(sa, sw0);
             sab1 = __fmul_rn(sa, sw1);
+          }
+          if (!mbar_wait(tfull_bar(b), (c >> 1) & 1, abort_flag, status)) {
+            ok = false;
+            break;
           }
           tc_fence_after_sync();
           if (qlive) {
