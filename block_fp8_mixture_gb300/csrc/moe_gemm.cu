@@ -163,7 +163,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
       int sr0, sr1;
       bool has_sr1;
       scale_rows<kFC1>(p, w, sr0, sr1, has_sr1);
-      const int kb_end = (w.ks + 1) * kb_per_split;
       for (int st = 0; st < nst_item; ++st) {
         const int kbs = w.ks * kb_per_split + st * kPK;       // first K block of the stage
         const int s = sc % kStages;
@@ -278,7 +277,8 @@ __global__ void __launch_bounds__(kTileThreads, 1)
         const uint8_t* slot = slots + sl * kScaleSlotBytes;
         for (int k = 0; k < nv; ++k) {
           const int b = c & 1;
-          // the scales need only their slot: read them before waiting for the partial sums
+          // the scales need only their slot: read them before waiting for the partial sums, and
+          // give the slot back to the producer once the stage's last K block has read them
           if (k == 0 && !mbar_wait(sfull_bar(sl), (sc / kSlots) & 1, abort_flag, status)) {
             ok = false;
             break;
@@ -292,6 +292,10 @@ __global__ void __launch_bounds__(kTileThreads, 1)
                                       : 0.0f;
             sab0 = __fmul_rn(sa, sw0);
             sab1 = __fmul_rn(sa, sw1);
+          }
+          if (k == nv - 1) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sempty_bar(sl));   // this warp has read the stage's scales
           }
           if (!mbar_wait(tfull_bar(b), (c >> 1) & 1, abort_flag, status)) {
             ok = false;
@@ -315,8 +319,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           ++c;
         }
         if (!ok) break;
-        __syncwarp();
-        if (lane == 0) mbar_arrive(sempty_bar(sl));   // this warp has read the stage's scales
         ++sc;
       }
       if (!ok) break;
