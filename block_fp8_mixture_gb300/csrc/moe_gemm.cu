@@ -283,15 +283,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
             ok = false;
             break;
           }
-          float sab0 = 0.0f, sab1 = 0.0f;
+          // loads only: their values are first used after the wait below
+          float sa = 0.0f, sw0 = 0.0f, sw1 = 0.0f;
           if (qlive) {
-            const float sa = smem_scale_at(slot + k * a_kb_bytes, row, a_ue);
             const int i0 = sr0 * KB + kbs, i1 = sr1 * KB + kbs;
-            const float sw0 = smem_scale_at(slot + kSlotW, (i0 & w_mask) + k, b_ue);
-            const float sw1 = has_sr1 ? smem_scale_at(slot + kSlotW + 128, (i1 & w_mask) + k, b_ue)
-                                      : 0.0f;
-            sab0 = __fmul_rn(sa, sw0);
-            sab1 = __fmul_rn(sa, sw1);
+            sa = smem_scale_at(slot + k * a_kb_bytes, row, a_ue);
+            sw0 = smem_scale_at(slot + kSlotW, (i0 & w_mask) + k, b_ue);
+            if (has_sr1) sw1 = smem_scale_at(slot + kSlotW + 128, (i1 & w_mask) + k, b_ue);
           }
           if (k == nv - 1) {
             __syncwarp();
@@ -303,6 +301,7 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           }
           tc_fence_after_sync();
           if (qlive) {
+            const float sab0 = __fmul_rn(sa, sw0), sab1 = __fmul_rn(sa, sw1);
             const uint32_t t0 = tmem_base + ((uint32_t)(q * 32) << 16) + b * kBN;
             if (kFC1) {
               promote64(t0 + wg * 64, t0 + wg * 64 + 32, sab0, acc);
