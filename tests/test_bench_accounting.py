@@ -62,3 +62,5 @@ def test_reference_arm_reports_the_same_config():
     assert line["config"] == bench.bench_config(synth.SHAPES["tiny"], 16, 16, 1)
     assert line["value"] > 0 and line["cpu_baseline"]["value"] == line["value"]
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+    # a step is one sampled token: its wall time, not the layer time it scales to
+    assert line["ms_per_step"] * 1e3 * 16 == pytest.approx(line["value"])
