@@ -193,7 +193,7 @@ def test_layer_maximum_dimensions(E, H, I, topk, M, n, small, ksplit):
 
 
 @pytest.mark.parametrize("clamp_mode,limit", [(0, 0.0), (1, 0.02), (2, 0.01)])
-@pytest.mark.parametrize("act_fmt,weight_fmt", [(0, 0), (1, 0), (2, 2)])
+@pytest.mark.parametrize("act_fmt,weight_fmt", [(0, 0), (1, 0), (2, 2), (0, 2), (2, 0)])
 def test_layer_tile_kernel_variants(clamp_mode, limit, act_fmt, weight_fmt):
     """128-row-tile schedule (P_cap > 16 E): odd K-block counts (I = 384), a hidden size that
     ends on half an output tile (H = 384), and a device token count below capacity."""
@@ -222,8 +222,12 @@ def test_layer_decode_reciprocal_numerics():
     _layer_check(synth.make_case("decode_r", 4, shape=shape))
 
 
-def test_layer_small_ue8m0_weights():
-    shape = synth.small_shape("small_u", E=10, H=1024, I=256, topk=4, act_fmt=2, weight_fmt=2)
+@pytest.mark.parametrize("act_fmt,weight_fmt", [(2, 2), (0, 2), (2, 0), (1, 2)])
+def test_layer_small_ue8m0_weights(act_fmt, weight_fmt):
+    """Small-batch schedule with UE8M0 block scales on either operand (byte scales: 16 to a
+    16-byte scale box) and mixed with fp32 or power-of-two fp32 scales on the other."""
+    shape = synth.small_shape("small_u", E=10, H=1024, I=256, topk=4, act_fmt=act_fmt,
+                              weight_fmt=weight_fmt)
     _layer_check(synth.make_case("small_u", 64, shape=shape))
 
 
