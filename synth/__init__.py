@@ -14,6 +14,8 @@ Workload shapes follow the pages' benchmark shapes, scaled to synthetic data:
   padded     E=32  H=7168 I=2048 k=8  capacity 512 / 16 live, 4096 / 4096 live, UE8M0
   glm_slice  E=256 H=6144 I=256  k=8  M in {1,8,64,256,1024,4096}, Zipf(1.2) routing
   mid        E=128 H=2048 I=768  k=8  M in {1,8,32,128,512,2048,8192}, 1% outliers x10
+  glm_slice_pow2  glm_slice with power-of-two-rounded fp32 activation scales
+  mid_empty       mid with every fourth expert never routed to
 """
 
 from __future__ import annotations
@@ -63,6 +65,12 @@ SHAPES = {
     "padded_fp32": LayerShape("padded_fp32", 32, 7168, 2048, 8, cfg_id=3),
     "glm_slice": LayerShape("glm_slice", 256, 6144, 256, 8, routing="zipf", cfg_id=4),
     "mid": LayerShape("mid", 128, 2048, 768, 8, routing="softmax", outliers=0.01, cfg_id=5),
+    # the variants the two swept configurations also name: power-of-two-rounded activation scales,
+    # and routing with forced-empty experts (every fourth expert never chosen)
+    "glm_slice_pow2": LayerShape("glm_slice_pow2", 256, 6144, 256, 8, act_fmt=SCALE_FP32_POW2,
+                                 routing="zipf", cfg_id=4),
+    "mid_empty": LayerShape("mid_empty", 128, 2048, 768, 8, routing="softmax_empty4",
+                            outliers=0.01, cfg_id=5),
 }
 
 # M values of each workload (capacity, live) pairs
@@ -73,6 +81,8 @@ SWEEPS = {
     "padded_fp32": [(512, 16), (4096, 4096)],
     "glm_slice": [(m, m) for m in (1, 8, 64, 256, 1024, 4096)],
     "mid": [(m, m) for m in (1, 8, 32, 128, 512, 2048, 8192)],
+    "glm_slice_pow2": [(m, m) for m in (1, 8, 64, 256, 1024, 4096)],
+    "mid_empty": [(m, m) for m in (1, 8, 32, 128, 512, 2048, 8192)],
 }
 
 
