@@ -23,7 +23,7 @@
 //   warp 1 (one lane)  MMA issuer: per K block 4 tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32;
 //                      4 x 2 with N=128 when a stage holds two K blocks) into one of two
 //                      256-column fp32 accumulators in tensor memory.
-//   warps 4..11        promotion + epilogue (224 registers after setmaxnreg).  A thread owns one
+//   warps 4..11        promotion + epilogue (232 registers after setmaxnreg).  A thread owns one
 //                      row and 128 of the 256 columns; per K block it reads its partial sums from
 //                      tensor memory (two loads in flight per wait) and accumulates
 //                      acc = fma(partial, a_scale*b_scale, acc) in registers, then releases the

@@ -32,12 +32,13 @@ constexpr int kABoxRows = 8;                          // activation rows per TMA
 constexpr int kGemmThreads = 320;                     // small kernel: TMA, MMA, 8 epilogue warps
 constexpr int kSmallPK = 2;                           // small kernel: K blocks per operand stage
 constexpr int kEpiWarp0 = 2;
-// 128-row-tile kernel: warpgroup 0 = TMA warp, MMA warp, two idle warps (56 registers each after
-// setmaxnreg); warpgroups 1-2 = the 8 promotion/epilogue warps (224 registers each).
+// 128-row-tile kernel: warpgroup 0 = TMA warp, MMA warp, two idle warps (40 registers each after
+// setmaxnreg); warpgroups 1-2 = the 8 promotion/epilogue warps (232 registers each: 128
+// accumulators, 64 loaded partial sums and the loop state without spills).
 constexpr int kTileThreads = 384;
 constexpr int kTileEpiWarp0 = 4;
-constexpr int kTileRegsLow = 56;
-constexpr int kTileRegsHigh = 224;
+constexpr int kTileRegsLow = 40;
+constexpr int kTileRegsHigh = 232;
 static_assert(128 * kTileRegsLow + 256 * kTileRegsHigh <= kTileThreads * 168,
               "register split must fit the launch allocation");
 static_assert(32 * (kTileRegsLow + 2 * kTileRegsHigh) <= 16384, "register split per sub-partition");
