@@ -13,16 +13,15 @@
 // blockIdx.x + gridDim.x, ...; inside the CTA:
 //   warp 0 (one lane)  TMA producer.  Each stage of the operand ring receives the tile's 128
 //                      activation rows (one 5-D box that also permutes the 8-row groups, below)
-//                      and its 256 weight rows (one box, 128-byte swizzle) for one or two 128-wide
-//                      K blocks; a separate, deeper ring of scale slots receives the stage's
+//                      and its 256 weight rows (one box, 128-byte swizzle) for one 128-wide K
+//                      block; a separate, deeper ring of scale slots receives the stage's
 //                      activation scales (one 2-D box) and two 32-byte boxes of weight block
 //                      scales.  Five copies per stage.  The MMA releases an operand stage on
 //                      completion, the promotion warps release the scale slot once they have
 //                      read it.  Rows of a tile past the expert's live end are loaded too (they
 //                      stay inside the workspace) and their results are discarded.
-//   warp 1 (one lane)  MMA issuer: per K block 4 tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32;
-//                      4 x 2 with N=128 when a stage holds two K blocks) into one of two
-//                      256-column fp32 accumulators in tensor memory.
+//   warp 1 (one lane)  MMA issuer: per K block 4 tcgen05.mma kind::f8f6f4 (M=128, N=256, K=32)
+//                      into one of two 256-column fp32 accumulators in tensor memory.
 //   warps 4..11        promotion + epilogue (232 registers after setmaxnreg).  A thread owns one
 //                      row and 128 of the 256 columns; per K block it reads its partial sums from
 //                      tensor memory (two loads in flight per wait) and accumulates
@@ -41,7 +40,6 @@
 
 namespace moe {
 
-constexpr uint32_t kIdesc = make_idesc_e4m3(kBM, kGroup);   // M = 128, N = 128 per MMA
 // M = 128, N = 256: one MMA per K step when the two weight halves are contiguous (one K block per
 // stage); about 520 cycles per 128x256x128 K block against about 770 for two N = 128 MMAs
 constexpr uint32_t kIdesc256 = make_idesc_e4m3(kBM, 2 * kGroup);
@@ -207,7 +205,6 @@ __global__ void __launch_bounds__(kTileThreads, 1)
     bool ok = true;
     for (int item = blockIdx.x; ok && item < total; item += gridDim.x) {
       const Item w = decode_item(p, item);
-      const bool second = kFC1 || (w.nb * kBN + kGroup) < p.out_cols;
       const int kb_end = (w.ks + 1) * kb_per_split;
       for (int st = 0; ok && st < nst_item; ++st) {
         const int kbs = w.ks * kb_per_split + st * kPK;
@@ -228,18 +225,13 @@ __global__ void __launch_bounds__(kTileThreads, 1)
           tc_fence_after_sync();
           const uint32_t d = tmem_base + b * kBN;
           const uint64_t adesc = make_sdesc_sw128(sA + k * (kABoxRows * kBK), kABoxRows * kBK * kPK);
-          const uint64_t g_desc = make_sdesc_sw128(sB + k * (kGroup * kBK));
-          const uint64_t u_desc = make_sdesc_sw128(sB + kBHalfBytes + k * (kGroup * kBK));
+          static_assert(kPK == 1, "one K block per stage: the two weight halves are contiguous");
+          // both 128-row weight halves (gate and up, or low and high) are contiguous: one N = 256
+          // MMA per K step
+          const uint64_t b_desc = make_sdesc_sw128(sB + k * (kGroup * kBK));
 #pragma unroll
-          for (int kk = 0; kk < kBK / 32; ++kk) {
-            if constexpr (kPK == 1) {
-              // both 128-row weight halves are contiguous: one N = 256 MMA per K step
-              mma_f8(d, adesc + 2 * kk, g_desc + 2 * kk, kIdesc256, kk > 0 ? 1u : 0u);
-            } else {
-              mma_f8(d, adesc + 2 * kk, g_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
-              if (second) mma_f8(d + kGroup, adesc + 2 * kk, u_desc + 2 * kk, kIdesc, kk > 0 ? 1u : 0u);
-            }
-          }
+          for (int kk = 0; kk < kBK / 32; ++kk)
+            mma_f8(d, adesc + 2 * kk, b_desc + 2 * kk, kIdesc256, kk > 0 ? 1u : 0u);
           mma_commit(tfull_bar(b));
           ++c;
         }

@@ -51,21 +51,20 @@ constexpr int kTmemCols = 512;                        // two 256-column accumula
 // boxes (which cover the stage's K blocks) at kSlotW and kSlotW + 128
 constexpr int kSlotW = 1024;
 constexpr int kSlotBytes = kSlotW + 256;
-constexpr int kMaxPK = 2;
 
-// Pipeline shape of the 128-row-tile kernels.  FC1 (long K, small output) of the promotion kernel
-// streams two K blocks per stage (256-byte runs per row) through two stages; the block-scaled FC1
-// (kBS), whose MMAs release a stage without waiting for a promotion, streams one K block per stage
-// through four (measured 6% faster there, 1% slower with promotion).  FC2 (short K, a 64 KB BF16
-// output tile per item) uses one K block per stage, three stages, and a 64 KB staging area from
-// which asynchronous TMA stores write the output tile while the next item proceeds.
+// Pipeline shape of the 128-row-tile kernels: one K block per stage, so each K block's gate and up
+// (or low and high) weight rows sit together and one N = 256 MMA covers them.  FC1 (long K, small
+// output) streams through four stages.  FC2 (short K, a 64 KB BF16 output tile per item) uses three
+// stages and a 64 KB staging area from which asynchronous TMA stores write the output tile while
+// the next item proceeds (the block-scaled FC2: four stages and 2 KB of staging per warp).  Two K
+// blocks per stage, tried for the promotion kernel's FC1, made its promotion warps spill registers.
 template <bool kFC1, bool kBS = false>
 struct TileCfg {
-  static constexpr int PK = (kFC1 && !kBS) ? 2 : 1;
+  static constexpr int PK = 1;
   // FC2 of the block-scaled kernel stores its output one 8-row group at a time through 2 KB per warp,
   // which leaves room for a fourth operand stage
   static constexpr bool YByGroup = !kFC1 && kBS;
-  static constexpr int Stages = kFC1 ? (kBS ? 4 : 2) : (YByGroup ? 4 : 3);
+  static constexpr int Stages = kFC1 ? 4 : (YByGroup ? 4 : 3);
   static constexpr int ABytes = kBM * kBK * PK;
   static constexpr int BHalf = kGroup * kBK * PK;     // 128 weight rows
   static constexpr int StageBytes = ABytes + 2 * BHalf;
